@@ -1,0 +1,214 @@
+/*
+ * pka.h — batched attention between a ragged query tensor and a paged KV
+ * cache in CSR form, as a plan/run C ABI for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (sources are cited by page title and section):
+ *
+ *   For request r with Q = qo_len[r] query rows and K = kv_len[r] keys,
+ *     O[i, h]   = sum_j softmax_j(scale * q_i,h . k_j,h/g + mask) v_j,h/g
+ *     LSE[i, h] = log2( sum_{visible j} exp(scale * q_i,h . k_j,h/g) )
+ *   with g = num_qo_heads / num_kv_heads (qo head h reads kv head h / g).
+ *   - "Deep Dive - FlashInfer", "Why inference attention becomes irregular":
+ *     qo_indptr counts query rows; kv_indptr counts page ids; the length
+ *     contract K = page_size * (pages - 1) + last_page_len, 1 <= last <= P;
+ *     K already includes the tokens appended this step.
+ *   - same page, "Causality uses logical positions, not page numbers":
+ *     logical key j lives in page kv_indices[kv_indptr[r] + j / P], slot
+ *     j % P; causal rows see keys j <= K - Q + i (bottom-right aligned).
+ *   - same page, "Core mechanism" and "A worked split-KV example": the state
+ *     (o, b) with b the base-2 log of the natural-exp sum; states over
+ *     disjoint key ranges merge exactly (normalised scales first).
+ *   - same page, "Plan then run": a host plan per batch, a run per layer.
+ *   - "KV-Cache layouts" (FlashInfer docs): "NHD/HND" page layouts, "Ragged
+ *     Tensor" (kv_indptr over tokens), "Mask layout (2D Ragged Tensor)"
+ *     (per-request row-major masks at mask_indptr = cumsum(qo_len * kv_len),
+ *     bit-packed 8 per byte, little-endian), "Page table layout" (5-D or
+ *     tuple K/V storage; the caller owns the page table).
+ *
+ * Conventions for every call:
+ *   - Payloads (q, k, v, o, k_new, v_new) are bfloat16; lse is float32 in
+ *     base-2 units; index arrays are int32.
+ *   - "_h" pointers are host memory, "_d" and payload pointers device memory.
+ *   - The library allocates no device or host memory.  The caller owns every
+ *     buffer; pka_plan_create allocates the small host plan object (and one
+ *     CUDA event on the first pka_plan with a device workspace).
+ *   - All device work is ordered on the caller's stream, passed as a
+ *     cudaStream_t cast to void* (NULL = legacy default stream).
+ *   - Every call returns a pka_status; nothing throws across the ABI and no
+ *     kernel traps.  Kernels that wait on a barrier give up after a bounded
+ *     number of polls and record PKA_ERR_DEVICE_TIMEOUT, readable with
+ *     pka_get_device_error.
+ */
+#ifndef PKA_H_
+#define PKA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKA_VERSION_MAJOR 1
+#define PKA_VERSION_MINOR 0
+
+typedef enum pka_status {
+  PKA_OK = 0,
+  PKA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad enum        */
+  PKA_ERR_METADATA = 2,       /* indptr / last_page_len violate the contract  */
+  PKA_ERR_UNSUPPORTED = 3,    /* head_dim, head ratio or mode not built       */
+  PKA_ERR_WORKSPACE = 4,      /* a workspace or staging buffer is too small   */
+  PKA_ERR_STALE_PLAN = 5,     /* run() parameters differ from plan()'s        */
+  PKA_ERR_CUDA = 6,           /* a CUDA runtime call failed                   */
+  PKA_ERR_DEVICE_TIMEOUT = 7  /* a kernel gave up waiting on a barrier        */
+} pka_status;
+
+typedef enum pka_layout { PKA_NHD = 0, PKA_HND = 1 } pka_layout;
+typedef enum pka_mask_mode {
+  PKA_MASK_NONE = 0,
+  PKA_MASK_CAUSAL = 1,  /* key j visible to local row i iff j <= K - Q + i   */
+  PKA_MASK_CUSTOM = 2   /* bit mask_indptr[r] + i*K + j of the packed mask; */
+                        /* 1 keeps the key, 0 drops it                       */
+} pka_mask_mode;
+typedef enum pka_split_mode {
+  PKA_SPLIT_OFF = 0,    /* one work item per (request, head block, q tile)   */
+  PKA_SPLIT_AUTO = 1,   /* planner balances keys across CTAs, merges splits  */
+  PKA_SPLIT_FIXED = 2   /* every key range cut into fixed_split_pages pages  */
+} pka_split_mode;
+
+typedef struct pka_params {
+  int32_t num_qo_heads;      /* Hq >= 1                                        */
+  int32_t num_kv_heads;      /* Hk >= 1, Hq % Hk == 0, Hq / Hk in {1,2,4,8}    */
+  int32_t head_dim;          /* D in {64, 128}                                 */
+  int32_t page_size;         /* P >= 1 (ignored when kv_ragged)               */
+  int32_t layout;            /* pka_layout of the K/V pages                    */
+  int32_t mask_mode;         /* pka_mask_mode                                  */
+  float sm_scale;            /* <= 0 selects 1/sqrt(D)                         */
+  int32_t kv_ragged;         /* 1: K/V are ragged [tokens, Hk, D] tensors and  */
+                             /*    kv_indptr counts tokens ("Ragged Tensor")   */
+  int32_t split_mode;        /* pka_split_mode                                 */
+  int32_t fixed_split_pages; /* pages per chunk for PKA_SPLIT_FIXED (>= 1)     */
+  int32_t num_sms;           /* 0: query the current device; > 0: plan for it  */
+  int32_t reserved[5];       /* must be zero                                   */
+} pka_params;
+
+/* Summary of a plan, filled by pka_plan (also when it fails with
+ * PKA_ERR_WORKSPACE, so a caller can size its buffers and call again). */
+typedef struct pka_plan_info {
+  uint64_t int_ws_bytes;     /* device int workspace and pinned staging bytes  */
+  uint64_t float_ws_bytes;   /* float workspace pka_run needs (split states)   */
+  int32_t num_requests;
+  int32_t nnz_qo;            /* qo_indptr[batch]                               */
+  int64_t total_kv;          /* sum of kv_len over requests                    */
+  int32_t num_decode_ctas;   /* CTAs of the decode launch (qo_len == 1 rows)   */
+  int32_t num_decode_items;
+  int32_t num_prefill_ctas;  /* CTAs of the tensor-core launch (qo_len >= 2)   */
+  int32_t num_prefill_items;
+  int32_t num_merge_tasks;   /* (row, qo head) pairs merged after a split     */
+  int32_t num_partial_records;
+  int32_t decode_chunk_tokens; /* keys per decode CTA (0: no split)            */
+  int32_t reserved[5];
+} pka_plan_info;
+
+typedef struct pka_plan_s* pka_plan_t;
+
+/* Static description of an error code. Never NULL. */
+const char* pka_status_str(pka_status status);
+
+/* Library version (PKA_VERSION_MAJOR / MINOR). */
+pka_status pka_version(int32_t* major, int32_t* minor);
+
+/* Check the batch description against the contract without planning.
+ * qo_indptr_h may be NULL (decode: one row per request).  Host only; needs
+ * no GPU.  Returns PKA_ERR_METADATA for: indptr[0] != 0, a decreasing
+ * indptr, a request with no page, last_page_len outside 1..P, causal rows
+ * with kv_len < qo_len; PKA_ERR_UNSUPPORTED for head_dim not in {64,128} or a
+ * head ratio not in {1,2,4,8}; PKA_ERR_INVALID_ARG for bad enums or sizes. */
+pka_status pka_validate(const pka_params* params, int32_t batch, const int32_t* qo_indptr_h,
+                        const int32_t* kv_indptr_h, const int32_t* last_page_len_h);
+
+/* Create / destroy the host plan object. */
+pka_status pka_plan_create(pka_plan_t* plan);
+void pka_plan_destroy(pka_plan_t plan);
+
+/* plan(): inspect one batch on the host ("Deep Dive - FlashInfer", "Plan
+ * then run"; "Load balancing and split-KV decisions").
+ *   Validates the metadata, derives kv_len, mask offsets, query tiles with
+ *   GQA row packing, split-KV chunks and the merge list, writes the plan
+ *   image into pinned_h and copies it into int_ws_d with cudaMemcpyAsync on
+ *   `stream`.  kv_indices is not read here: pka_run reads it on the device, so
+ *   pages may be remapped between runs without a new plan as long as the
+ *   lengths stay the same.
+ *   int_ws_d == NULL: host-only dry run (no CUDA call; pinned_h may be any
+ *   host memory).  Needs info.int_ws_bytes of both int_ws_d and pinned_h; on
+ *   a short buffer returns PKA_ERR_WORKSPACE with the sizes in the plan info.
+ *   pinned_h must stay untouched until the copy completes: call
+ *   pka_plan_wait before reusing it for another plan. */
+pka_status pka_plan(pka_plan_t plan, const pka_params* params, int32_t batch,
+                    const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
+                    const int32_t* last_page_len_h, void* int_ws_d, size_t int_ws_bytes,
+                    void* pinned_h, size_t pinned_bytes, void* stream);
+
+/* Copy the plan's summary into *info. */
+pka_status pka_plan_get_info(pka_plan_t plan, pka_plan_info* info);
+
+/* Block until the plan's host-to-device copy has completed. */
+pka_status pka_plan_wait(pka_plan_t plan);
+
+/* run(): execute the plan for one layer.
+ *   q   [nnz_qo, Hq, D] bf16, o [nnz_qo, Hq, D] bf16, lse [nnz_qo, Hq] fp32
+ *   (lse may be NULL).
+ *   Paged K/V: k and v point at page 0 of the K and V pools; page p starts
+ *   page_stride elements after page p-1 (NHD page [P, Hk, D], HND page
+ *   [Hk, P, D]).  5-D storage [pages, 2, ...] passes k = base, v = base +
+ *   P*Hk*D and page_stride = 2*P*Hk*D; tuple storage passes page_stride =
+ *   P*Hk*D.  Ragged K/V: k, v are [kv_indptr[batch], Hk, D]; page_stride and
+ *   kv_indices_d are ignored.
+ *   packed_mask_d: little-endian bit array, read only for PKA_MASK_CUSTOM.
+ *   float_ws_d: at least info.float_ws_bytes (may be NULL when that is 0).
+ *   Returns PKA_ERR_STALE_PLAN when *params differs from the planned one. */
+pka_status pka_run(pka_plan_t plan, const pka_params* params, const void* q, const void* k,
+                   const void* v, int64_t page_stride, const int32_t* kv_indices_d,
+                   const uint8_t* packed_mask_d, void* o, float* lse, void* float_ws_d,
+                   size_t float_ws_bytes, void* stream);
+
+/* append_paged_kv_cache ("KV-Cache layouts", "Page table layout": pages of
+ * the appended rows are allocated beforehand by the caller).
+ *   Request r appends rows append_indptr_d[r] .. append_indptr_d[r+1] of
+ *   k_new/v_new [nnz_new, Hk, D]; its kv_len (from kv_indptr_d and
+ *   last_page_len_d) already counts them, so row t lands at logical position
+ *   kv_len - n_append + t.  Uses params->num_kv_heads, head_dim, page_size and
+ *   layout.  Device metadata is trusted (not validated); nnz_new must equal
+ *   append_indptr_d[batch]. */
+pka_status pka_append_paged_kv_cache(const pka_params* params, int32_t batch, const void* k_new,
+                                     const void* v_new, const int32_t* append_indptr_d,
+                                     int64_t nnz_new, const int32_t* kv_indptr_d,
+                                     const int32_t* kv_indices_d,
+                                     const int32_t* last_page_len_d, void* k, void* v,
+                                     int64_t page_stride, void* stream);
+
+/* merge_states ("Deep Dive - FlashInfer", "A worked split-KV example"):
+ *   For every row r and head h, merge the states s = indptr_d[r] ..
+ *   indptr_d[r+1]-1 of v [S, heads, dim] (fp32, each normalised over its own
+ *   keys) with statistics lse [S, heads] (base 2).  Empty states (lse = -inf)
+ *   are skipped; a row with no finite state yields zeros and -inf.  Writes
+ *   v_out [rows, heads, dim] bf16 and lse_out [rows, heads] fp32 (may be
+ *   NULL).  dim in {64, 128}. */
+pka_status pka_merge_states(const float* v, const float* lse, const int32_t* indptr_d,
+                            int32_t rows, int32_t heads, int32_t dim, void* v_out,
+                            float* lse_out, void* stream);
+
+/* packbits ("KV-Cache layouts", "Mask layout (2D Ragged Tensor)"): element
+ * k of bools_d (non-zero = 1) becomes bit (k & 7) of byte k >> 3 of out_d;
+ * the unused high bits of the last byte are 0.  out_d holds (n + 7) / 8 bytes. */
+pka_status pka_packbits(const uint8_t* bools_d, int64_t n, uint8_t* out_d, void* stream);
+
+/* Read and clear the device error word written by kernels that gave up on a
+ * barrier (0 = none, else a pka_status).  Synchronises `stream`. */
+pka_status pka_get_device_error(int32_t* code, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKA_H_ */

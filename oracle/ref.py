@@ -104,13 +104,14 @@ def mask_indptr(qo_lens, kv_lens) -> list[int]:
 
 
 def packbits_little(bools) -> np.ndarray:
-    """Pack 0/1 values 8 per byte, element k -> bit (k & 7) of byte k >> 3."""
-    flat = [1 if int(x) else 0 for x in np.asarray(bools).reshape(-1)]
-    out = np.zeros((len(flat) + 7) // 8, dtype=np.uint8)
-    for k, bit in enumerate(flat):
-        if bit:
-            out[k >> 3] |= np.uint8(1 << (k & 7))
-    return out
+    """Pack 0/1 values 8 per byte, element k -> bit (k & 7) of byte k >> 3.
+
+    Non-zero counts as 1; the high bits of a short last byte are 0."""
+    flat = (np.asarray(bools).reshape(-1) != 0).astype(np.uint16)
+    padded = np.zeros(((flat.size + 7) // 8) * 8, dtype=np.uint16)
+    padded[:flat.size] = flat
+    weights = np.array([1 << k for k in range(8)], dtype=np.uint16)  # bit k of each byte
+    return (padded.reshape(-1, 8) * weights).sum(axis=1).astype(np.uint8)
 
 
 def mask_bit(packed, k: int) -> bool:
@@ -239,12 +240,13 @@ def visible_keys(mode, i, qo_len, kv_len, packed_mask=None, mask_start=0):
 def batch_attention(q_bits, k_pool_bits, v_pool_bits, *, qo_indptr, kv_indptr, kv_indices,
                     last_page_len, page_size, num_qo_heads, num_kv_heads, layout="NHD",
                     mask_mode="causal", packed_mask=None, sm_scale=None, kv_ragged=False,
-                    requests=None, kv_range=None):
+                    requests=None, kv_range=None, rows=None):
     """Reference output of one batch.
 
     Returns (o, lse2) as float64 arrays [nnz_q, Hq, D] and [nnz_q, Hq]; rows of
     requests not listed in ``requests`` stay NaN.  ``kv_range`` (t0, t1)
-    restricts every request to logical keys t0 <= j < t1 (a split-KV chunk)."""
+    restricts every request to logical keys t0 <= j < t1 (a split-KV chunk).
+    ``rows`` (a set of global query rows) computes only those rows."""
     q = bf16_bits_to_f64(q_bits)
     head_dim = q.shape[-1]
     if num_qo_heads % num_kv_heads:
@@ -266,6 +268,8 @@ def batch_attention(q_bits, k_pool_bits, v_pool_bits, *, qo_indptr, kv_indptr, k
             continue
         if mask_mode == "causal" and klen < qlen:
             raise ValueError("causal attention needs kv_len >= qo_len")
+        if rows is not None and not any(int(qo_indptr[r]) + i in rows for i in range(qlen)):
+            continue
         kr = bf16_bits_to_f64(gather_request_kv(
             k_pool_bits, layout=layout, page_size=page_size, kv_indptr=kv_indptr,
             kv_indices=kv_indices, req=r, kv_len=klen, kv_ragged=kv_ragged))
@@ -274,6 +278,8 @@ def batch_attention(q_bits, k_pool_bits, v_pool_bits, *, qo_indptr, kv_indptr, k
             kv_indices=kv_indices, req=r, kv_len=klen, kv_ragged=kv_ragged))
         for i in range(qlen):
             row = int(qo_indptr[r]) + i
+            if rows is not None and row not in rows:
+                continue
             keys = visible_keys(mask_mode, i, qlen, klen, packed_mask, m_indptr[r])
             if kv_range is not None:
                 keys = [j for j in keys if kv_range[0] <= j < kv_range[1]]

@@ -1,0 +1,79 @@
+"""Batched attention between a ragged query tensor and a paged KV cache
+(CSR page table) on NVIDIA GB300, behind a plan/run C ABI (``libpka.so``).
+
+``_pka`` mirrors the C entry points one to one; ``BatchAttention`` below only
+owns the workspaces those calls need (device int workspace, pinned staging
+buffer, device float workspace) and forwards to them.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _pka
+from ._pka import (PKA_HND, PKA_MASK_CAUSAL, PKA_MASK_CUSTOM, PKA_MASK_NONE, PKA_NHD,  # noqa
+                   PKA_SPLIT_AUTO, PKA_SPLIT_FIXED, PKA_SPLIT_OFF, PkaError, make_params,
+                   pka_append_paged_kv_cache, pka_get_device_error, pka_merge_states,
+                   pka_packbits, pka_plan, pka_plan_create, pka_plan_destroy, pka_plan_get_info,
+                   pka_plan_wait, pka_run, pka_status_str, pka_validate, pka_version)
+
+__all__ = ["BatchAttention", "make_params", "PkaError"] + [n for n in _pka.EXPORTED]
+
+_WORKSPACE = 4
+
+
+class BatchAttention:
+    """Plan once per batch, run once per layer (the pages' plan/run contract)."""
+
+    def __init__(self, device="cuda", int_ws_bytes=1 << 20, float_ws_bytes=16 << 20):
+        _pka.lib()
+        self.device = torch.device(device)
+        self.handle = pka_plan_create()
+        self.int_ws = torch.empty(int_ws_bytes, dtype=torch.uint8, device=self.device)
+        self.pinned = torch.empty(int_ws_bytes, dtype=torch.uint8, pin_memory=True)
+        self.float_ws = torch.empty(float_ws_bytes, dtype=torch.uint8, device=self.device)
+        self.params = None
+        self.info = None
+
+    def __del__(self):
+        try:
+            pka_plan_destroy(self.handle)
+        except Exception:
+            pass
+
+    def plan(self, qo_indptr, kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, head_dim,
+             page_size=1, layout="NHD", mask_mode="causal", sm_scale=0.0, kv_ragged=False,
+             split_mode="auto", fixed_split_pages=1, num_sms=0, stream=None):
+        params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, layout, mask_mode,
+                             sm_scale, kv_ragged, split_mode, fixed_split_pages, num_sms)
+        s = pka_plan(self.handle, params, qo_indptr, kv_indptr, last_page_len, self.int_ws,
+                     self.pinned, stream, check=False)
+        if s == _WORKSPACE:
+            info = pka_plan_get_info(self.handle)
+            pka_plan_wait(self.handle)
+            n = max(int(info.int_ws_bytes), self.int_ws.numel())
+            self.int_ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+            self.pinned = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+            s = pka_plan(self.handle, params, qo_indptr, kv_indptr, last_page_len, self.int_ws,
+                         self.pinned, stream, check=False)
+        if s != 0:
+            raise PkaError(s, "pka_plan")
+        self.params = params
+        self.info = pka_plan_get_info(self.handle)
+        if self.info.float_ws_bytes > self.float_ws.numel():
+            self.float_ws = torch.empty(int(self.info.float_ws_bytes), dtype=torch.uint8,
+                                        device=self.device)
+        return self.info
+
+    def run(self, q, k, v, kv_indices=None, packed_mask=None, *, page_stride=None, out=None,
+            lse=None, return_lse=True, stream=None):
+        if self.params is None:
+            raise RuntimeError("plan() before run()")
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None and return_lse:
+            lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+        if page_stride is None:
+            page_stride = k.stride(0) if not self.params.kv_ragged else 0
+        pka_run(self.handle, self.params, q, k, v, page_stride, kv_indices, packed_mask, out, lse,
+                self.float_ws, stream)
+        return out, lse

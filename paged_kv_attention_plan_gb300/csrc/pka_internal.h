@@ -1,0 +1,80 @@
+// Internal declarations shared by the host entry points and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pka.h"
+#include "pka_plan_image.h"
+
+namespace pka {
+
+// Everything one attention launch needs besides its work list.
+struct AttnArgs {
+  const int32_t* cta_ptr;     // [num_ctas + 1] item ranges per CTA
+  const PkaWorkItem* items;
+  const uint16_t* q;          // bf16 bits [nnz_q, Hq, D]
+  const uint16_t* k;          // bf16 bits, pool or ragged tensor
+  const uint16_t* v;
+  int64_t page_stride;        // elements between consecutive pages
+  const int32_t* kv_indices;  // page ids (paged only)
+  const uint8_t* mask;        // packed custom mask (custom mode only)
+  uint16_t* o;                // bf16 bits [nnz_q, Hq, D]
+  float* lse;                 // [nnz_q, Hq] or null
+  float* part_o;              // [records, D] partial outputs (normalised)
+  float* part_lse;            // [records]
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t page_size;
+  int32_t layout;             // PKA_NHD / PKA_HND
+  int32_t kv_ragged;
+  int32_t mask_mode;
+  int32_t heads_per_cta;      // decode: kv heads a CTA covers
+  float scale_log2;           // sm_scale * log2(e)
+  int32_t* err;               // device error word (bounded waits that gave up)
+};
+
+struct MergeArgs {
+  const PkaMergeTask* tasks;  // plan merge list (tasks == null -> indptr mode)
+  int32_t num_tasks;
+  const int32_t* indptr;      // merge_states mode: [rows + 1]
+  int32_t rows;
+  int32_t heads;
+  const float* part_o;        // [records, D]
+  const float* part_lse;      // [records]
+  uint16_t* o;                // bf16 bits [rows, heads, D]
+  float* lse;                 // [rows, heads] or null
+  int32_t head_dim;
+};
+
+cudaError_t launch_decode(const AttnArgs& a, int num_ctas, int head_dim, int group,
+                          cudaStream_t stream);
+cudaError_t launch_prefill(const AttnArgs& a, int num_ctas, int head_dim, int group,
+                           cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+cudaError_t launch_packbits(const uint8_t* in, int64_t n, uint8_t* out, cudaStream_t stream);
+cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_new,
+                          const uint16_t* v_new, const int32_t* append_indptr, int64_t nnz,
+                          const int32_t* kv_indptr, const int32_t* kv_indices,
+                          const int32_t* last_page_len, uint16_t* k, uint16_t* v,
+                          int64_t page_stride, cudaStream_t stream);
+cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
+// Device address of the error word on the current device (null on failure).
+int32_t* device_error_word();
+
+// Decode launch geometry shared by the planner and the kernel.
+// A decode CTA covers `heads_per_cta` kv heads; each kv head is served by
+// `warps_per_kv_head` consumer warps of up to 4 qo heads each.
+inline int decode_warps_per_kv_head(int group) { return group > 4 ? group / 4 : 1; }
+inline int decode_heads_per_cta(int num_kv_heads, int group) {
+  int wph = decode_warps_per_kv_head(group);
+  int h = 8 / wph;
+  if (h > num_kv_heads) h = num_kv_heads;
+  while (h > 1 && num_kv_heads % h) --h;
+  return h;
+}
+
+constexpr int kDecodeTileTokens = 16;   // keys per pipeline stage of the decode kernel
+constexpr int kPrefillTileKeys = 128;   // keys per tensor-core tile
+constexpr int kPrefillTileRows = 128;   // packed (token, qo head) rows per tile
+
+}  // namespace pka

@@ -1,0 +1,64 @@
+// Layout of the plan image that pka_plan writes into the pinned staging
+// buffer and copies into the caller's device int workspace.  Shared by the
+// host planner and the kernels (both are the product path).
+//
+// image := header | decode_cta_ptr | decode_items | prefill_cta_ptr |
+//          prefill_items | merge_tasks          (all offsets in int32 units)
+#pragma once
+#include <stdint.h>
+
+#define PKA_IMAGE_MAGIC 0x31414B50  // "PKA1"
+
+struct PkaImageHeader {
+  int32_t magic;
+  int32_t total_words;           // size of the whole image in int32 words
+  int32_t num_decode_ctas;
+  int32_t num_decode_items;
+  int32_t num_prefill_ctas;
+  int32_t num_prefill_items;
+  int32_t num_merge_tasks;
+  int32_t num_partial_records;
+  int32_t off_decode_cta_ptr;    // int32[num_decode_ctas + 1]
+  int32_t off_decode_items;      // PkaWorkItem[num_decode_items]
+  int32_t off_prefill_cta_ptr;   // int32[num_prefill_ctas + 1]
+  int32_t off_prefill_items;     // PkaWorkItem[num_prefill_items]
+  int32_t off_merge_tasks;       // PkaMergeTask[num_merge_tasks]
+  int32_t decode_heads_per_cta;  // kv heads one decode CTA covers
+  int32_t reserved[2];
+};
+
+// One unit of attention work: a block of kv heads (decode) or one kv head
+// (tensor-core path), a tile of query tokens of one request, and a key range.
+struct PkaWorkItem {
+  int32_t req;
+  int32_t kv_head0;    // first kv head
+  int32_t n_kv_heads;  // kv heads covered
+  int32_t q_row0;      // global row of the tile's first query token
+  int32_t q_local0;    // its index i inside the request (0..qo_len-1)
+  int32_t q_count;     // query tokens in the tile
+  int32_t qo_len;      // Q of the request
+  int32_t kv_len;      // K of the request
+  int32_t kv_base;     // kv_indptr[req]: first page id slot (or first token if ragged)
+  int32_t t0;          // first key of the range (logical position)
+  int32_t t1;          // one past the last key
+  int32_t out_rec;     // -1: write O/LSE; else first partial record ([token][qo head])
+  int32_t mask_lo;     // mask_indptr[req] (bit offset), low/high words
+  int32_t mask_hi;
+  int32_t flags;
+  int32_t reserved;
+};
+
+// One (query row, qo head) whose partial states are merged after a split.
+// Record k (0 <= k < nslots) of the task is rec_first + k * rec_stride.
+struct PkaMergeTask {
+  int32_t out_row;
+  int32_t head;
+  int32_t rec_first;
+  int32_t nslots;
+  int32_t rec_stride;
+  int32_t reserved[3];
+};
+
+static_assert(sizeof(PkaImageHeader) == 64, "header size");
+static_assert(sizeof(PkaWorkItem) == 64, "work item size");
+static_assert(sizeof(PkaMergeTask) == 32, "merge task size");

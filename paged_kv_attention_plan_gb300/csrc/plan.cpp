@@ -1,0 +1,593 @@
+// Host side of the C ABI: metadata validation, the planner (work partition,
+// split-KV chunking, merge list) and the run / utility entry points.
+//
+// The planner follows "Deep Dive - FlashInfer", sections "Plan then run"
+// (inspect the irregular metadata once per batch on the host, copy the work
+// list to the device asynchronously, run a stable kernel per layer) and
+// "Load balancing and split-KV decisions" (partition long key ranges across
+// CTAs, merge their partial states).  The pages give no split threshold; the
+// policy here is ours (see split_decode / split_prefill below).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <vector>
+
+#include "pka_internal.h"
+
+using pka::AttnArgs;
+
+struct pka_plan_s {
+  pka_params params{};
+  bool planned = false;
+  pka_plan_info info{};
+  PkaImageHeader hdr{};
+  int32_t* int_ws_d = nullptr;
+  cudaEvent_t event = nullptr;
+  bool copy_pending = false;
+  int device = -1;
+};
+
+namespace {
+
+constexpr int kMinDecodeChunk = 64;
+
+bool params_ok(const pka_params* p) {
+  if (!p) return false;
+  for (int i = 0; i < 5; ++i)
+    if (p->reserved[i] != 0) return false;
+  if (p->num_qo_heads < 1 || p->num_kv_heads < 1) return false;
+  if (p->layout != PKA_NHD && p->layout != PKA_HND) return false;
+  if (p->mask_mode < PKA_MASK_NONE || p->mask_mode > PKA_MASK_CUSTOM) return false;
+  if (p->split_mode < PKA_SPLIT_OFF || p->split_mode > PKA_SPLIT_FIXED) return false;
+  if (p->split_mode == PKA_SPLIT_FIXED && p->fixed_split_pages < 1) return false;
+  if (!p->kv_ragged && p->page_size < 1) return false;
+  if (p->num_sms < 0) return false;
+  return true;
+}
+
+pka_status check_supported(const pka_params* p) {
+  if (p->num_qo_heads % p->num_kv_heads) return PKA_ERR_UNSUPPORTED;
+  int g = p->num_qo_heads / p->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return PKA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128) return PKA_ERR_UNSUPPORTED;
+  return PKA_OK;
+}
+
+struct Batch {
+  std::vector<int32_t> qo_len, kv_len, q_row0, kv_base;
+  std::vector<int64_t> mask_base;
+  int64_t total_kv = 0;
+  int32_t nnz_q = 0;
+};
+
+// Length contract of "Why inference attention becomes irregular" and the
+// "Page table layout" section: K = P * (pages - 1) + last, 1 <= last <= P.
+pka_status derive(const pka_params* p, int32_t batch, const int32_t* qo, const int32_t* kv,
+                  const int32_t* last, Batch* b) {
+  if (batch < 0 || !kv || (!p->kv_ragged && !last)) return PKA_ERR_INVALID_ARG;
+  if (kv[0] != 0) return PKA_ERR_METADATA;
+  if (qo && qo[0] != 0) return PKA_ERR_METADATA;
+  b->qo_len.resize(batch);
+  b->kv_len.resize(batch);
+  b->q_row0.resize(batch);
+  b->kv_base.resize(batch);
+  b->mask_base.resize(batch + 1);
+  b->mask_base[0] = 0;
+  int64_t rows = 0;
+  for (int32_t r = 0; r < batch; ++r) {
+    int64_t npages = (int64_t)kv[r + 1] - kv[r];
+    if (npages < 0) return PKA_ERR_METADATA;
+    int64_t klen;
+    if (p->kv_ragged) {
+      klen = npages;
+    } else {
+      if (npages < 1) return PKA_ERR_METADATA;
+      if (last[r] < 1 || last[r] > p->page_size) return PKA_ERR_METADATA;
+      klen = (int64_t)p->page_size * (npages - 1) + last[r];
+    }
+    if (klen > INT32_MAX) return PKA_ERR_UNSUPPORTED;
+    int64_t qlen = qo ? (int64_t)qo[r + 1] - qo[r] : 1;
+    if (qlen < 0) return PKA_ERR_METADATA;
+    if (p->mask_mode == PKA_MASK_CAUSAL && klen < qlen) return PKA_ERR_METADATA;
+    b->qo_len[r] = (int32_t)qlen;
+    b->kv_len[r] = (int32_t)klen;
+    b->q_row0[r] = (int32_t)(qo ? qo[r] : r);
+    b->kv_base[r] = kv[r];
+    b->total_kv += klen;
+    rows += qlen;
+    if (rows > INT32_MAX) return PKA_ERR_UNSUPPORTED;
+    b->mask_base[r + 1] = b->mask_base[r] + qlen * klen;
+  }
+  b->nnz_q = (int32_t)rows;
+  return PKA_OK;
+}
+
+PkaWorkItem make_item(const Batch& b, int r, int kv_head0, int n_kv_heads, int q_local0,
+                      int q_count, int t0, int t1) {
+  PkaWorkItem it{};
+  it.req = r;
+  it.kv_head0 = kv_head0;
+  it.n_kv_heads = n_kv_heads;
+  it.q_row0 = b.q_row0[r] + q_local0;
+  it.q_local0 = q_local0;
+  it.q_count = q_count;
+  it.qo_len = b.qo_len[r];
+  it.kv_len = b.kv_len[r];
+  it.kv_base = b.kv_base[r];
+  it.t0 = t0;
+  it.t1 = t1;
+  it.out_rec = -1;
+  it.mask_lo = (int32_t)(uint32_t)(b.mask_base[r] & 0xffffffffu);
+  it.mask_hi = (int32_t)(b.mask_base[r] >> 32);
+  return it;
+}
+
+struct PlanLists {
+  std::vector<int32_t> dec_cta_ptr{0};
+  std::vector<PkaWorkItem> dec_items;
+  std::vector<int32_t> pre_cta_ptr{0};
+  std::vector<PkaWorkItem> pre_items;
+  std::vector<PkaMergeTask> merges;
+  int32_t records = 0;
+  int32_t decode_chunk = 0;
+};
+
+// Give the pieces of one split unit their partial records and merge tasks.
+// `pieces` index into `items`; each piece writes q_count * heads records laid
+// out [token][qo head]; the heads are heads_total qo heads starting at head0.
+void assign_records(PlanLists* L, std::vector<PkaWorkItem>& items,
+                    const std::vector<int>& pieces, int q_row0, int q_count, int head0,
+                    int heads_total) {
+  if (pieces.size() < 2) return;
+  int per = q_count * heads_total;
+  int base = L->records;
+  for (size_t k = 0; k < pieces.size(); ++k) items[pieces[k]].out_rec = base + (int)k * per;
+  for (int i = 0; i < q_count; ++i)
+    for (int h = 0; h < heads_total; ++h) {
+      PkaMergeTask t{};
+      t.out_row = q_row0 + i;
+      t.head = head0 + h;
+      t.rec_first = base + i * heads_total + h;
+      t.nslots = (int)pieces.size();
+      t.rec_stride = per;
+      L->merges.push_back(t);
+    }
+  L->records += (int)pieces.size() * per;
+}
+
+// Decode rows (qo_len == 1): units are (request, block of kv heads); with
+// split AUTO the keys of all units are dealt out in equal shares to one
+// persistent CTA per SM (a unit may span CTAs, a CTA may hold several units).
+void plan_decode(const pka_params* p, const Batch& b, int num_sms, PlanLists* L) {
+  int g = p->num_qo_heads / p->num_kv_heads;
+  int hpc = pka::decode_heads_per_cta(p->num_kv_heads, g);
+  int hg_count = p->num_kv_heads / hpc;
+  struct Unit { int r, hg, K; };
+  std::vector<Unit> units;
+  int64_t total = 0;
+  for (int r = 0; r < (int)b.qo_len.size(); ++r) {
+    if (b.qo_len[r] != 1) continue;
+    for (int hg = 0; hg < hg_count; ++hg) {
+      units.push_back({r, hg, b.kv_len[r]});
+      total += b.kv_len[r];
+    }
+  }
+  if (units.empty()) return;
+  int64_t chunk = 0;
+  if (p->split_mode == PKA_SPLIT_FIXED) {
+    chunk = (int64_t)p->fixed_split_pages * (p->kv_ragged ? 1 : p->page_size);
+  } else if (p->split_mode == PKA_SPLIT_AUTO) {
+    int64_t target = (total + num_sms - 1) / num_sms;
+    target = (target + pka::kDecodeTileTokens - 1) / pka::kDecodeTileTokens * pka::kDecodeTileTokens;
+    chunk = std::max<int64_t>(target, kMinDecodeChunk);
+  }
+  L->decode_chunk = (int)chunk;
+  auto& items = L->dec_items;
+  if (p->split_mode != PKA_SPLIT_AUTO) {
+    // one CTA per piece
+    for (const Unit& u : units) {
+      std::vector<int> pieces;
+      int64_t step = chunk > 0 ? chunk : std::max(u.K, 1);
+      int64_t t = 0;
+      do {
+        int64_t t1 = std::min<int64_t>(u.K, t + step);
+        pieces.push_back((int)items.size());
+        items.push_back(make_item(b, u.r, u.hg * hpc, hpc, 0, 1, (int)t, (int)t1));
+        L->dec_cta_ptr.push_back((int)items.size());
+        t = t1;
+      } while (t < u.K);
+      assign_records(L, items, pieces, b.q_row0[u.r], 1, u.hg * hpc * g, hpc * g);
+    }
+    return;
+  }
+  int64_t load = 0;
+  for (const Unit& u : units) {
+    std::vector<int> pieces;
+    int64_t t = 0;
+    do {
+      int64_t take = std::min<int64_t>(u.K - t, chunk - load);
+      pieces.push_back((int)items.size());
+      items.push_back(make_item(b, u.r, u.hg * hpc, hpc, 0, 1, (int)t, (int)(t + take)));
+      t += take;
+      load += take;
+      if (load >= chunk) {
+        L->dec_cta_ptr.push_back((int)items.size());
+        load = 0;
+      }
+    } while (t < u.K);
+    assign_records(L, items, pieces, b.q_row0[u.r], 1, u.hg * hpc * g, hpc * g);
+  }
+  if (L->dec_cta_ptr.back() != (int)items.size()) L->dec_cta_ptr.push_back((int)items.size());
+}
+
+// Rows of requests with qo_len >= 2 go to the tensor-core kernel: units are
+// (request, kv head, tile of 128 / g query tokens) so that the g qo heads of
+// one kv head pack into a 128-row tile and share every K/V load.  Causal
+// units only visit keys up to the tile's last visible one.  Items are dealt
+// to CTAs longest-first onto the least loaded CTA.
+void plan_prefill(const pka_params* p, const Batch& b, int num_sms, PlanLists* L) {
+  int g = p->num_qo_heads / p->num_kv_heads;
+  int tq = pka::kPrefillTileRows / g;
+  struct Unit { int r, h, q0, qc, kend; };
+  std::vector<Unit> units;
+  int64_t total_tiles = 0;
+  for (int r = 0; r < (int)b.qo_len.size(); ++r) {
+    int Q = b.qo_len[r], K = b.kv_len[r];
+    if (Q < 2) continue;
+    for (int h = 0; h < p->num_kv_heads; ++h)
+      for (int q0 = 0; q0 < Q; q0 += tq) {
+        int qc = std::min(tq, Q - q0);
+        int kend = K;
+        if (p->mask_mode == PKA_MASK_CAUSAL) kend = K - Q + (q0 + qc - 1) + 1;
+        units.push_back({r, h, q0, qc, kend});
+        total_tiles += (kend + pka::kPrefillTileKeys - 1) / pka::kPrefillTileKeys;
+      }
+  }
+  if (units.empty()) return;
+  int64_t chunk = 0;  // keys per piece, 0 = whole range
+  if (p->split_mode == PKA_SPLIT_FIXED) {
+    chunk = (int64_t)p->fixed_split_pages * (p->kv_ragged ? 1 : p->page_size);
+  } else if (p->split_mode == PKA_SPLIT_AUTO && (int64_t)units.size() < 2 * num_sms) {
+    int64_t per_cta = std::max<int64_t>(4, (total_tiles + num_sms - 1) / num_sms);
+    chunk = per_cta * pka::kPrefillTileKeys;
+  }
+  auto& items = L->pre_items;
+  std::vector<int64_t> cost;
+  for (const Unit& u : units) {
+    std::vector<int> pieces;
+    int64_t step = chunk > 0 ? chunk : std::max(u.kend, 1);
+    int64_t t = 0;
+    do {
+      int64_t t1 = std::min<int64_t>(u.kend, t + step);
+      pieces.push_back((int)items.size());
+      items.push_back(make_item(b, u.r, u.h, 1, u.q0, u.qc, (int)t, (int)t1));
+      cost.push_back((t1 - t) + 64);
+      t = t1;
+    } while (t < u.kend);
+    assign_records(L, items, pieces, b.q_row0[u.r] + u.q0, u.qc, u.h * g, g);
+  }
+  int n = (int)items.size();
+  int ctas = std::min(n, num_sms);
+  std::vector<int> order(n);
+  for (int i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return cost[a] > cost[c]; });
+  using Slot = std::pair<int64_t, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push({0, c});
+  std::vector<std::vector<int>> per(ctas);
+  for (int i : order) {
+    Slot s = heap.top();
+    heap.pop();
+    per[s.second].push_back(i);
+    heap.push({s.first + cost[i], s.second});
+  }
+  std::vector<PkaWorkItem> sorted;
+  sorted.reserve(n);
+  for (int c = 0; c < ctas; ++c) {
+    for (int i : per[c]) sorted.push_back(items[i]);
+    L->pre_cta_ptr.push_back((int)sorted.size());
+  }
+  items.swap(sorted);
+}
+
+size_t align_words(size_t w) { return (w + 15) & ~size_t(15); }
+
+}  // namespace
+
+extern "C" {
+
+const char* pka_status_str(pka_status s) {
+  switch (s) {
+    case PKA_OK: return "ok";
+    case PKA_ERR_INVALID_ARG: return "invalid argument";
+    case PKA_ERR_METADATA: return "metadata violates the indptr / page-table contract";
+    case PKA_ERR_UNSUPPORTED: return "unsupported head_dim, head ratio or mode";
+    case PKA_ERR_WORKSPACE: return "workspace or staging buffer too small";
+    case PKA_ERR_STALE_PLAN: return "run parameters differ from the planned ones";
+    case PKA_ERR_CUDA: return "CUDA runtime error";
+    case PKA_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on a barrier";
+  }
+  return "unknown status";
+}
+
+pka_status pka_version(int32_t* major, int32_t* minor) {
+  if (!major || !minor) return PKA_ERR_INVALID_ARG;
+  *major = PKA_VERSION_MAJOR;
+  *minor = PKA_VERSION_MINOR;
+  return PKA_OK;
+}
+
+pka_status pka_validate(const pka_params* p, int32_t batch, const int32_t* qo,
+                        const int32_t* kv, const int32_t* last) {
+  if (!params_ok(p)) return PKA_ERR_INVALID_ARG;
+  pka_status s = check_supported(p);
+  if (s != PKA_OK) return s;
+  Batch b;
+  return derive(p, batch, qo, kv, last, &b);
+}
+
+pka_status pka_plan_create(pka_plan_t* plan) {
+  if (!plan) return PKA_ERR_INVALID_ARG;
+  *plan = new (std::nothrow) pka_plan_s();
+  return *plan ? PKA_OK : PKA_ERR_INVALID_ARG;
+}
+
+void pka_plan_destroy(pka_plan_t plan) {
+  if (!plan) return;
+  if (plan->event) {
+    cudaEventSynchronize(plan->event);
+    cudaEventDestroy(plan->event);
+  }
+  delete plan;
+}
+
+pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const int32_t* qo,
+                    const int32_t* kv, const int32_t* last, void* int_ws_d, size_t int_ws_bytes,
+                    void* pinned_h, size_t pinned_bytes, void* stream) {
+  if (!plan || !params_ok(p)) return PKA_ERR_INVALID_ARG;
+  plan->planned = false;
+  pka_status s = check_supported(p);
+  if (s != PKA_OK) return s;
+  Batch b;
+  s = derive(p, batch, qo, kv, last, &b);
+  if (s != PKA_OK) return s;
+
+  int num_sms = p->num_sms;
+  if (num_sms == 0) {
+    if (int_ws_d) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PKA_ERR_CUDA;
+    } else {
+      num_sms = 152;
+    }
+  }
+
+  PlanLists L;
+  plan_decode(p, b, num_sms, &L);
+  plan_prefill(p, b, num_sms, &L);
+
+  PkaImageHeader h{};
+  h.magic = PKA_IMAGE_MAGIC;
+  h.num_decode_ctas = (int)L.dec_cta_ptr.size() - 1;
+  h.num_decode_items = (int)L.dec_items.size();
+  h.num_prefill_ctas = (int)L.pre_cta_ptr.size() - 1;
+  h.num_prefill_items = (int)L.pre_items.size();
+  h.num_merge_tasks = (int)L.merges.size();
+  h.num_partial_records = L.records;
+  h.decode_heads_per_cta =
+      pka::decode_heads_per_cta(p->num_kv_heads, p->num_qo_heads / p->num_kv_heads);
+  size_t w = align_words(sizeof(PkaImageHeader) / 4);
+  h.off_decode_cta_ptr = (int)w;
+  w = align_words(w + L.dec_cta_ptr.size());
+  h.off_decode_items = (int)w;
+  w = align_words(w + L.dec_items.size() * (sizeof(PkaWorkItem) / 4));
+  h.off_prefill_cta_ptr = (int)w;
+  w = align_words(w + L.pre_cta_ptr.size());
+  h.off_prefill_items = (int)w;
+  w = align_words(w + L.pre_items.size() * (sizeof(PkaWorkItem) / 4));
+  h.off_merge_tasks = (int)w;
+  w = align_words(w + L.merges.size() * (sizeof(PkaMergeTask) / 4));
+  h.total_words = (int)w;
+
+  pka_plan_info info{};
+  info.int_ws_bytes = (uint64_t)w * 4;
+  size_t rec_o = (size_t)L.records * p->head_dim * 4;
+  size_t rec_o_al = (rec_o + 255) & ~size_t(255);
+  info.float_ws_bytes = L.records ? rec_o_al + (((size_t)L.records * 4 + 255) & ~size_t(255)) : 0;
+  info.num_requests = batch;
+  info.nnz_qo = b.nnz_q;
+  info.total_kv = b.total_kv;
+  info.num_decode_ctas = h.num_decode_ctas;
+  info.num_decode_items = h.num_decode_items;
+  info.num_prefill_ctas = h.num_prefill_ctas;
+  info.num_prefill_items = h.num_prefill_items;
+  info.num_merge_tasks = h.num_merge_tasks;
+  info.num_partial_records = L.records;
+  info.decode_chunk_tokens = L.decode_chunk;
+  plan->info = info;
+  if (!pinned_h || pinned_bytes < info.int_ws_bytes) return PKA_ERR_WORKSPACE;
+  if (int_ws_d && int_ws_bytes < info.int_ws_bytes) return PKA_ERR_WORKSPACE;
+
+  // The pinned buffer may still feed a previous copy of this plan object.
+  if (plan->copy_pending && plan->event) {
+    if (cudaEventSynchronize(plan->event) != cudaSuccess) return PKA_ERR_CUDA;
+    plan->copy_pending = false;
+  }
+  int32_t* img = static_cast<int32_t*>(pinned_h);
+  std::memset(img, 0, info.int_ws_bytes);
+  std::memcpy(img, &h, sizeof(h));
+  std::memcpy(img + h.off_decode_cta_ptr, L.dec_cta_ptr.data(), L.dec_cta_ptr.size() * 4);
+  if (!L.dec_items.empty())
+    std::memcpy(img + h.off_decode_items, L.dec_items.data(), L.dec_items.size() * sizeof(PkaWorkItem));
+  std::memcpy(img + h.off_prefill_cta_ptr, L.pre_cta_ptr.data(), L.pre_cta_ptr.size() * 4);
+  if (!L.pre_items.empty())
+    std::memcpy(img + h.off_prefill_items, L.pre_items.data(), L.pre_items.size() * sizeof(PkaWorkItem));
+  if (!L.merges.empty())
+    std::memcpy(img + h.off_merge_tasks, L.merges.data(), L.merges.size() * sizeof(PkaMergeTask));
+
+  plan->params = *p;
+  plan->hdr = h;
+  plan->int_ws_d = static_cast<int32_t*>(int_ws_d);
+  if (int_ws_d) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!plan->event) {
+      if (cudaEventCreateWithFlags(&plan->event, cudaEventDisableTiming) != cudaSuccess)
+        return PKA_ERR_CUDA;
+    }
+    if (cudaMemcpyAsync(int_ws_d, img, info.int_ws_bytes, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+      return PKA_ERR_CUDA;
+    if (cudaEventRecord(plan->event, st) != cudaSuccess) return PKA_ERR_CUDA;
+    plan->copy_pending = true;
+  }
+  plan->planned = true;
+  return PKA_OK;
+}
+
+pka_status pka_plan_get_info(pka_plan_t plan, pka_plan_info* info) {
+  if (!plan || !info) return PKA_ERR_INVALID_ARG;
+  *info = plan->info;
+  return PKA_OK;
+}
+
+pka_status pka_plan_wait(pka_plan_t plan) {
+  if (!plan) return PKA_ERR_INVALID_ARG;
+  if (plan->copy_pending && plan->event) {
+    if (cudaEventSynchronize(plan->event) != cudaSuccess) return PKA_ERR_CUDA;
+    plan->copy_pending = false;
+  }
+  return PKA_OK;
+}
+
+pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const void* k,
+                   const void* v, int64_t page_stride, const int32_t* kv_indices,
+                   const uint8_t* mask, void* o, float* lse, void* float_ws, size_t float_ws_bytes,
+                   void* stream) {
+  if (!plan || !p || !plan->planned) return PKA_ERR_INVALID_ARG;
+  if (std::memcmp(&plan->params, p, sizeof(pka_params)) != 0) return PKA_ERR_STALE_PLAN;
+  if (!plan->int_ws_d) return PKA_ERR_INVALID_ARG;  // a host-only (dry-run) plan cannot run
+  if (!q || !k || !v || !o) return PKA_ERR_INVALID_ARG;
+  if (!p->kv_ragged && (!kv_indices || page_stride <= 0)) return PKA_ERR_INVALID_ARG;
+  // 16-byte alignment of every row the kernels move with vector or bulk copies
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((mis & 15) || (!p->kv_ragged && (page_stride & 7))) return PKA_ERR_INVALID_ARG;
+  if (p->mask_mode == PKA_MASK_CUSTOM && !mask) return PKA_ERR_INVALID_ARG;
+  if (float_ws_bytes < plan->info.float_ws_bytes || (plan->info.float_ws_bytes && !float_ws))
+    return PKA_ERR_WORKSPACE;
+  const PkaImageHeader& h = plan->hdr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int g = p->num_qo_heads / p->num_kv_heads;
+  float scale = p->sm_scale > 0.f ? p->sm_scale : 1.0f / std::sqrt((float)p->head_dim);
+  size_t rec_o = (size_t)h.num_partial_records * p->head_dim * 4;
+  size_t rec_o_al = (rec_o + 255) & ~size_t(255);
+
+  AttnArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.page_stride = page_stride;
+  a.kv_indices = kv_indices;
+  a.mask = mask;
+  a.o = static_cast<uint16_t*>(o);
+  a.lse = lse;
+  a.part_o = static_cast<float*>(float_ws);
+  a.part_lse = float_ws ? reinterpret_cast<float*>(static_cast<char*>(float_ws) + rec_o_al) : nullptr;
+  a.num_qo_heads = p->num_qo_heads;
+  a.num_kv_heads = p->num_kv_heads;
+  a.page_size = p->kv_ragged ? 1 : p->page_size;
+  a.layout = p->layout;
+  a.kv_ragged = p->kv_ragged;
+  a.mask_mode = p->mask_mode;
+  a.heads_per_cta = h.decode_heads_per_cta;
+  a.scale_log2 = scale * 1.4426950408889634f;
+
+  if (h.num_decode_items > 0) {
+    a.cta_ptr = plan->int_ws_d + h.off_decode_cta_ptr;
+    a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_decode_items);
+    if (pka::launch_decode(a, h.num_decode_ctas, p->head_dim, g, st) != cudaSuccess)
+      return PKA_ERR_CUDA;
+  }
+  if (h.num_prefill_items > 0) {
+    a.cta_ptr = plan->int_ws_d + h.off_prefill_cta_ptr;
+    a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_prefill_items);
+    if (pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g, st) != cudaSuccess)
+      return PKA_ERR_CUDA;
+  }
+  if (h.num_merge_tasks > 0) {
+    pka::MergeArgs m{};
+    m.tasks = reinterpret_cast<const PkaMergeTask*>(plan->int_ws_d + h.off_merge_tasks);
+    m.num_tasks = h.num_merge_tasks;
+    m.heads = p->num_qo_heads;
+    m.part_o = a.part_o;
+    m.part_lse = a.part_lse;
+    m.o = a.o;
+    m.lse = lse;
+    m.head_dim = p->head_dim;
+    if (pka::launch_merge(m, st) != cudaSuccess) return PKA_ERR_CUDA;
+  }
+  return PKA_OK;
+}
+
+pka_status pka_append_paged_kv_cache(const pka_params* p, int32_t batch, const void* k_new,
+                                     const void* v_new, const int32_t* append_indptr,
+                                     int64_t nnz_new, const int32_t* kv_indptr,
+                                     const int32_t* kv_indices, const int32_t* last_page_len,
+                                     void* k, void* v, int64_t page_stride, void* stream) {
+  if (!params_ok(p) || batch < 0 || nnz_new < 0) return PKA_ERR_INVALID_ARG;
+  if (p->head_dim != 64 && p->head_dim != 128) return PKA_ERR_UNSUPPORTED;
+  if (p->kv_ragged) return PKA_ERR_UNSUPPORTED;
+  if (nnz_new == 0 || batch == 0) return PKA_OK;
+  if (!k_new || !v_new || !append_indptr || !kv_indptr || !kv_indices || !last_page_len || !k ||
+      !v || page_stride <= 0)
+    return PKA_ERR_INVALID_ARG;
+  if (pka::launch_append(*p, batch, static_cast<const uint16_t*>(k_new),
+                         static_cast<const uint16_t*>(v_new), append_indptr, nnz_new, kv_indptr,
+                         kv_indices, last_page_len, static_cast<uint16_t*>(k),
+                         static_cast<uint16_t*>(v), page_stride,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKA_ERR_CUDA;
+  return PKA_OK;
+}
+
+pka_status pka_merge_states(const float* v, const float* lse, const int32_t* indptr,
+                            int32_t rows, int32_t heads, int32_t dim, void* v_out,
+                            float* lse_out, void* stream) {
+  if (rows < 0 || heads < 1) return PKA_ERR_INVALID_ARG;
+  if (dim != 64 && dim != 128) return PKA_ERR_UNSUPPORTED;
+  if (rows == 0) return PKA_OK;
+  if (!v || !lse || !indptr || !v_out) return PKA_ERR_INVALID_ARG;
+  pka::MergeArgs m{};
+  m.indptr = indptr;
+  m.rows = rows;
+  m.heads = heads;
+  m.part_o = v;
+  m.part_lse = lse;
+  m.o = static_cast<uint16_t*>(v_out);
+  m.lse = lse_out;
+  m.head_dim = dim;
+  return pka::launch_merge(m, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKA_OK
+                                                                                : PKA_ERR_CUDA;
+}
+
+pka_status pka_packbits(const uint8_t* in, int64_t n, uint8_t* out, void* stream) {
+  if (n < 0) return PKA_ERR_INVALID_ARG;
+  if (n == 0) return PKA_OK;
+  if (!in || !out) return PKA_ERR_INVALID_ARG;
+  return pka::launch_packbits(in, n, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKA_OK
+             : PKA_ERR_CUDA;
+}
+
+pka_status pka_get_device_error(int32_t* code, void* stream) {
+  if (!code) return PKA_ERR_INVALID_ARG;
+  return pka::read_and_clear_device_error(code, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKA_OK
+             : PKA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,222 @@
+// Bandwidth kernels around the attention launches: the state merge,
+// append_paged_kv_cache, packbits, and the device error word.
+#include <mutex>
+
+#include "pka_device.cuh"
+#include "pka_internal.h"
+
+namespace pka {
+
+// Written by kernels whose bounded barrier waits gave up (0 = no error).
+__device__ int32_t g_device_error;
+
+int32_t* device_error_word() {
+  static std::mutex mu;
+  static int32_t* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int32_t*>(p);
+  }
+  return cache[dev];
+}
+
+cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream) {
+  int32_t* p = device_error_word();
+  if (!p) return cudaErrorInvalidDevice;
+  int32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, p, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  *code = host;
+  if (host != 0) {
+    e = cudaMemsetAsync(p, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+  }
+  return e;
+}
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// State merge ("Deep Dive - FlashInfer", "A worked split-KV example"): the
+// n-way form of the two-way merge.  Shift by the largest finite statistic,
+// weight each state by 2^(b - shift), normalise the weights before the
+// weighted sum, and return shift + log2(sum of weights).  States with
+// b = -inf (no visible key) carry no weight; if every state is empty the
+// result is a zero vector and -inf.  One warp per (row, head).
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
+  constexpr int PER = D / 32;  // dims per lane
+  const int task = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  int out_row, head, rec_first, nslots, stride;
+  if (a.tasks) {
+    if (task >= a.num_tasks) return;
+    const PkaMergeTask t = a.tasks[task];
+    out_row = t.out_row;
+    head = t.head;
+    rec_first = t.rec_first;
+    nslots = t.nslots;
+    stride = t.rec_stride;
+  } else {
+    if (task >= a.rows * a.heads) return;
+    out_row = task / a.heads;
+    head = task % a.heads;
+    const int s0 = a.indptr[out_row], s1 = a.indptr[out_row + 1];
+    rec_first = s0 * a.heads + head;
+    nslots = s1 - s0;
+    stride = a.heads;
+  }
+  float shift = -INFINITY;
+  for (int k = 0; k < nslots; ++k) shift = fmaxf(shift, a.part_lse[(int64_t)rec_first + (int64_t)k * stride]);
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float z = 0.f;
+  if (shift != -INFINITY) {
+    for (int k = 0; k < nslots; ++k) z += exp2f(a.part_lse[(int64_t)rec_first + (int64_t)k * stride] - shift);
+    const float inv_z = 1.f / z;
+    for (int k = 0; k < nslots; ++k) {
+      const int64_t rec = (int64_t)rec_first + (int64_t)k * stride;
+      const float b = a.part_lse[rec];
+      if (b == -INFINITY) continue;
+      const float scale = exp2f(b - shift) * inv_z;
+      const float* src = a.part_o + rec * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += scale * x.x;
+        acc[1] += scale * x.y;
+        acc[2] += scale * x.z;
+        acc[3] += scale * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += scale * x.x;
+        acc[1] += scale * x.y;
+      }
+    }
+  }
+  uint16_t* dst = a.o + ((int64_t)out_row * a.heads + head) * D + lane * PER;
+  if constexpr (PER == 4) {
+    uint2 pk;
+    pk.x = float2_to_bf16x2(acc[0], acc[1]);
+    pk.y = float2_to_bf16x2(acc[2], acc[3]);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = float2_to_bf16x2(acc[0], acc[1]);
+  }
+  if (lane == 0 && a.lse)
+    a.lse[(int64_t)out_row * a.heads + head] = shift == -INFINITY ? -INFINITY : shift + log2f(z);
+}
+
+// ---------------------------------------------------------------------------
+// packbits ("KV-Cache layouts", "Mask layout (2D Ragged Tensor)"): element k
+// -> bit (k & 7) of byte k >> 3, little-endian within the byte.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) packbits_kernel(const uint8_t* __restrict__ in, int64_t n,
+                                                       uint8_t* __restrict__ out) {
+  const int64_t nbytes = (n + 7) >> 3;
+  for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nbytes;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t k0 = b << 3;
+    uint32_t byte = 0;
+    if (k0 + 8 <= n && ((reinterpret_cast<uintptr_t>(in + k0) & 7) == 0)) {
+      const uint2 x = *reinterpret_cast<const uint2*>(in + k0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        byte |= (((x.x >> (8 * i)) & 0xffu) != 0u) << i;
+        byte |= (((x.y >> (8 * i)) & 0xffu) != 0u) << (i + 4);
+      }
+    } else {
+      for (int i = 0; i < 8 && k0 + i < n; ++i) byte |= (in[k0 + i] != 0) << i;
+    }
+    out[b] = static_cast<uint8_t>(byte);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// append_paged_kv_cache ("KV-Cache layouts", "Page table layout"): appended
+// row t of request r goes to logical position kv_len - n_append + t, i.e.
+// page kv_indices[kv_indptr[r] + pos / P], slot pos % P.  One thread moves
+// 16 bytes of K and of V; the request of a row comes from a binary search of
+// append_indptr.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) append_kernel(
+    const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+    const int32_t* __restrict__ append_indptr, int32_t batch, int64_t nnz,
+    const int32_t* __restrict__ kv_indptr, const int32_t* __restrict__ kv_indices,
+    const int32_t* __restrict__ last_page_len, uint16_t* __restrict__ k,
+    uint16_t* __restrict__ v, int64_t page_stride, int hk, int d, int P, int layout) {
+  const int vec_per_head = d / 8;
+  const int64_t vec_per_row = (int64_t)hk * vec_per_head;
+  const int64_t total = nnz * vec_per_row;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = x / vec_per_row;
+    const int rem = (int)(x - row * vec_per_row);
+    const int h = rem / vec_per_head;
+    const int c = rem - h * vec_per_head;
+    int lo = 0, hi = batch - 1;  // last r with append_indptr[r] <= row
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (append_indptr[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const int r = lo;
+    const int n_app = append_indptr[r + 1] - append_indptr[r];
+    const int npages = kv_indptr[r + 1] - kv_indptr[r];
+    const int kv_len = (npages - 1) * P + last_page_len[r];
+    const int pos = kv_len - n_app + (int)(row - append_indptr[r]);
+    const int page = kv_indices[kv_indptr[r] + pos / P];
+    const int slot = pos % P;
+    int64_t dst = (int64_t)page * page_stride;
+    dst += layout == PKA_NHD ? ((int64_t)slot * hk + h) * d : ((int64_t)h * P + slot) * d;
+    dst += c * 8;
+    const int64_t src = (row * hk + h) * d + c * 8;
+    *reinterpret_cast<uint4*>(k + dst) = *reinterpret_cast<const uint4*>(k_new + src);
+    *reinterpret_cast<uint4*>(v + dst) = *reinterpret_cast<const uint4*>(v_new + src);
+  }
+}
+
+int grid_for(int64_t work, int block) {
+  int64_t g = (work + block - 1) / block;
+  if (g > 152 * 32) g = 152 * 32;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+  const int tasks = a.tasks ? a.num_tasks : a.rows * a.heads;
+  if (tasks <= 0) return cudaSuccess;
+  const int blocks = (tasks + 7) / 8;
+  if (a.head_dim == 128)
+    merge_kernel<128><<<blocks, 256, 0, stream>>>(a);
+  else
+    merge_kernel<64><<<blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_packbits(const uint8_t* in, int64_t n, uint8_t* out, cudaStream_t stream) {
+  packbits_kernel<<<grid_for((n + 7) / 8, 256), 256, 0, stream>>>(in, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_new,
+                          const uint16_t* v_new, const int32_t* append_indptr, int64_t nnz,
+                          const int32_t* kv_indptr, const int32_t* kv_indices,
+                          const int32_t* last_page_len, uint16_t* k, uint16_t* v,
+                          int64_t page_stride, cudaStream_t stream) {
+  const int64_t work = nnz * p.num_kv_heads * (p.head_dim / 8);
+  append_kernel<<<grid_for(work, 256), 256, 0, stream>>>(
+      k_new, v_new, append_indptr, batch, nnz, kv_indptr, kv_indices, last_page_len, k, v,
+      page_stride, p.num_kv_heads, p.head_dim, p.page_size, p.layout);
+  return cudaGetLastError();
+}
+
+}  // namespace pka

@@ -1,0 +1,74 @@
+"""Helpers for the GPU parity tests: move a seeded batch to the device, run
+it through the C ABI, and compare with the oracle."""
+import numpy as np
+import torch
+
+import paged_kv_attention_plan_gb300 as pka
+from oracle import ref
+
+# Parity bar: bf16 outputs within max-abs 2e-2 and mean-abs 2e-3 of the fp64
+# oracle, LSE (fp32, base 2) within 1e-4 absolute.
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-4
+
+
+def bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def i32(a, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def run_gpu(b, split=("auto", 1), packed_mask=None, attn=None, with_lse=True):
+    attn = attn or pka.BatchAttention()
+    qo = None if b.is_decode else b.qo_indptr
+    info = attn.plan(qo, b.kv_indptr, b.last_page_len, num_qo_heads=b.num_qo_heads,
+                     num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
+                     layout=b.layout, mask_mode=b.mask_mode, kv_ragged=b.kv_ragged,
+                     split_mode=split[0], fixed_split_pages=split[1])
+    q = bf16(b.q)
+    k, v = bf16(b.k_pool), bf16(b.v_pool)
+    idx = i32(b.kv_indices)
+    mask = None if packed_mask is None else torch.from_numpy(packed_mask).cuda()
+    o, lse = attn.run(q, k, v, idx, mask, return_lse=with_lse)
+    torch.cuda.synchronize()
+    assert pka.pka_get_device_error() == 0
+    return f64(o), (f64(lse) if with_lse else None), info
+
+
+def run_oracle(b, packed_mask=None, rows=None):
+    return ref.batch_attention(b.q, b.k_pool, b.v_pool, qo_indptr=b.qo_indptr,
+                               kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+                               last_page_len=b.last_page_len, page_size=b.page_size,
+                               num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                               layout=b.layout, mask_mode=b.mask_mode, packed_mask=packed_mask,
+                               sm_scale=b.sm_scale or None, kv_ragged=b.kv_ragged, rows=rows)
+
+
+def assert_parity(o, lse, o_ref, lse_ref, rows=None):
+    if rows is not None:
+        rows = sorted(rows)
+        o, o_ref = o[rows], o_ref[rows]
+        if lse is not None:
+            lse, lse_ref = lse[rows], lse_ref[rows]
+    assert np.all(np.isfinite(o_ref))
+    assert np.all(np.isfinite(o)), "non-finite output"
+    err = np.abs(o - o_ref)
+    assert err.max() <= O_MAX, f"max abs error {err.max():.3e}"
+    assert err.mean() <= O_MEAN, f"mean abs error {err.mean():.3e}"
+    if lse is not None:
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(fin, np.isfinite(lse)), "LSE -inf pattern differs"
+        if fin.any():
+            e = np.abs(lse[fin] - lse_ref[fin]).max()
+            assert e <= LSE_MAX, f"LSE max abs error {e:.3e}"
+        assert np.all(lse[~fin] == lse_ref[~fin])

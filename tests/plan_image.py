@@ -1,0 +1,30 @@
+"""Reader of the plan image (layout documented in csrc/pka_plan_image.h)."""
+import numpy as np
+
+HEADER = ["magic", "total_words", "num_decode_ctas", "num_decode_items", "num_prefill_ctas",
+          "num_prefill_items", "num_merge_tasks", "num_partial_records", "off_decode_cta_ptr",
+          "off_decode_items", "off_prefill_cta_ptr", "off_prefill_items", "off_merge_tasks",
+          "decode_heads_per_cta"]
+ITEM = ["req", "kv_head0", "n_kv_heads", "q_row0", "q_local0", "q_count", "qo_len", "kv_len",
+        "kv_base", "t0", "t1", "out_rec", "mask_lo", "mask_hi", "flags", "reserved"]
+MERGE = ["out_row", "head", "rec_first", "nslots", "rec_stride"]
+
+
+def parse(buf: np.ndarray):
+    w = np.frombuffer(buf.tobytes(), dtype=np.int32)
+    h = {k: int(w[i]) for i, k in enumerate(HEADER)}
+    assert h["magic"] == 0x31414B50
+
+    def items(off, n):
+        return [dict(zip(ITEM, map(int, w[off + 16 * i: off + 16 * (i + 1)]))) for i in range(n)]
+
+    dec_ptr = w[h["off_decode_cta_ptr"]: h["off_decode_cta_ptr"] + h["num_decode_ctas"] + 1]
+    pre_ptr = w[h["off_prefill_cta_ptr"]: h["off_prefill_cta_ptr"] + h["num_prefill_ctas"] + 1]
+    merges = [dict(zip(MERGE, map(int, w[h["off_merge_tasks"] + 8 * i:
+                                          h["off_merge_tasks"] + 8 * i + 5])))
+              for i in range(h["num_merge_tasks"])]
+    return {"header": h, "decode_cta_ptr": [int(x) for x in dec_ptr],
+            "decode_items": items(h["off_decode_items"], h["num_decode_items"]),
+            "prefill_cta_ptr": [int(x) for x in pre_ptr],
+            "prefill_items": items(h["off_prefill_items"], h["num_prefill_items"]),
+            "merges": merges}

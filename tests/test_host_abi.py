@@ -1,0 +1,288 @@
+"""Host-side tests of the C ABI: no GPU needed.
+
+The library loads and exports every entry point include/pka.h declares; the
+validator returns the documented status for each contract violation ("Deep
+Dive - FlashInfer", "Why inference attention becomes irregular": empty page
+list, tail outside 1..P; "KV-Cache layouts": int32 metadata); the planner's
+work list covers every (request, head block, query tile, key) exactly once,
+is deterministic, and reports workspace sizes.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_attention_plan_gb300 as pka
+from paged_kv_attention_plan_gb300 import _pka
+from paged_kv_attention_plan_gb300 import workloads as W
+from tests.plan_image import parse
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, METADATA, UNSUPPORTED, WORKSPACE, STALE = 0, 1, 2, 3, 4, 5
+
+
+def _i32(x):
+    return np.asarray(x, dtype=np.int32)
+
+
+def test_library_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "pka.h")).read()
+    declared = sorted(set(re.findall(r"\b(pka_[a-z_]+)\s*\(", header)))
+    assert declared, "no declarations found"
+    lib = _pka.lib()
+    missing = [name for name in declared if not hasattr(lib, name)]
+    assert not missing, missing
+    assert set(declared) == set(_pka.EXPORTED)
+
+
+def test_version_and_status_strings():
+    assert pka.pka_version() == (1, 0)
+    for code in range(8):
+        assert pka.pka_status_str(code)
+
+
+def _p(**kw):
+    base = dict(num_qo_heads=4, num_kv_heads=2, head_dim=64, page_size=4, num_sms=152)
+    base.update(kw)
+    return pka.make_params(**base)
+
+
+WORKED = (_i32([0, 3, 4, 8]), _i32([0, 2, 3, 6]), _i32([2, 2, 1]))
+
+
+def test_validate_worked_example():
+    assert pka.pka_validate(_p(), *WORKED) == OK
+
+
+@pytest.mark.parametrize("qo,kv,last,params,want", [
+    ([0, 3, 4, 8], [1, 2, 3, 6], [2, 2, 1], {}, METADATA),       # kv_indptr[0] != 0
+    ([1, 3, 4, 8], [0, 2, 3, 6], [2, 2, 1], {}, METADATA),       # qo_indptr[0] != 0
+    ([0, 3, 4, 8], [0, 2, 1, 6], [2, 2, 1], {}, METADATA),       # decreasing kv_indptr
+    ([0, 3, 2, 8], [0, 2, 3, 6], [2, 2, 1], {}, METADATA),       # decreasing qo_indptr
+    ([0, 3, 4, 8], [0, 2, 2, 6], [2, 2, 1], {}, METADATA),       # request without a page
+    ([0, 3, 4, 8], [0, 2, 3, 6], [2, 0, 1], {}, METADATA),       # tail 0
+    ([0, 3, 4, 8], [0, 2, 3, 6], [2, 5, 1], {}, METADATA),       # tail P + 1
+    ([0, 3, 6, 8], [0, 2, 3, 6], [2, 2, 1], {}, METADATA),       # causal with K=2 < Q=3
+    ([0, 3, 6, 8], [0, 2, 3, 6], [2, 2, 1], {"mask_mode": "none"}, OK),
+    ([0, 3, 4, 8], [0, 2, 3, 6], [2, 2, 1], {"num_qo_heads": 5}, UNSUPPORTED),
+    ([0, 3, 4, 8], [0, 2, 3, 6], [2, 2, 1], {"num_qo_heads": 6}, UNSUPPORTED),  # g = 3
+    ([0, 3, 4, 8], [0, 2, 3, 6], [2, 2, 1], {"head_dim": 96}, UNSUPPORTED),
+    ([0, 3, 4, 8], [0, 2, 3, 6], [2, 2, 1], {"layout": 7}, INVALID),
+    ([0, 3, 4, 8], [0, 2, 3, 6], [2, 2, 1], {"split_mode": "fixed", "fixed_split_pages": 0},
+     INVALID),
+])
+def test_validate_rejections(qo, kv, last, params, want):
+    assert pka.pka_validate(_p(**params), _i32(qo), _i32(kv), _i32(last)) == want
+
+
+def test_reserved_fields_must_be_zero():
+    p = _p()
+    p.reserved[2] = 1
+    assert pka.pka_validate(p, *WORKED) == INVALID
+
+
+def test_int64_metadata_rejected_by_binding():
+    with pytest.raises(TypeError):
+        pka.pka_validate(_p(), np.array([0, 3, 4, 8]), WORKED[1], WORKED[2])
+
+
+def _dry_plan(params, qo, kv, last):
+    h = pka.pka_plan_create()
+    try:
+        buf = np.zeros(64, np.uint8)
+        s = pka.pka_plan(h, params, qo, kv, last, None, buf, check=False)
+        info = pka.pka_plan_get_info(h)
+        if s == WORKSPACE:
+            buf = np.zeros(int(info.int_ws_bytes), np.uint8)
+            s = pka.pka_plan(h, params, qo, kv, last, None, buf, check=False)
+            info = pka.pka_plan_get_info(h)
+        assert s == OK, s
+        return parse(buf), info, buf
+    finally:
+        pka.pka_plan_destroy(h)
+
+
+def _ranges_tile(ranges, n):
+    ranges = sorted(ranges)
+    if n == 0:
+        return all(a == b == 0 for a, b in ranges)
+    pos = 0
+    for a, b in ranges:
+        if a != pos or b <= a:
+            return False
+        pos = b
+    return pos == n
+
+
+def check_coverage(plan, b, hq, hk, causal, info):
+    g = hq // hk
+    qo_len = np.diff(b.qo_indptr)
+    kv_len = np.asarray(b.kv_lens)
+    hpc = plan["header"]["decode_heads_per_cta"]
+    # every CTA has at least one item and the item lists tile the item array
+    for key in ("decode", "prefill"):
+        ptr = plan[f"{key}_cta_ptr"]
+        assert ptr[0] == 0 and ptr[-1] == len(plan[f"{key}_items"])
+        assert all(x < y for x, y in zip(ptr[:-1], ptr[1:]))
+    units = {}
+    for it in plan["decode_items"]:
+        assert qo_len[it["req"]] == 1 and it["q_count"] == 1 and it["n_kv_heads"] == hpc
+        units.setdefault((it["req"], it["kv_head0"]), []).append(it)
+    for r in np.nonzero(qo_len == 1)[0]:
+        for h0 in range(0, hk, hpc):
+            its = units.pop((int(r), h0))
+            assert _ranges_tile([(i["t0"], i["t1"]) for i in its], int(kv_len[r]))
+            assert all(i["q_row0"] == b.qo_indptr[r] for i in its)
+    assert not units
+    tq = 128 // g
+    for it in plan["prefill_items"]:
+        assert qo_len[it["req"]] >= 2 and it["n_kv_heads"] == 1
+        units.setdefault((it["req"], it["kv_head0"], it["q_local0"]), []).append(it)
+    for r in np.nonzero(qo_len >= 2)[0]:
+        Q, K = int(qo_len[r]), int(kv_len[r])
+        for h in range(hk):
+            for q0 in range(0, Q, tq):
+                its = units.pop((int(r), h, q0))
+                qc = min(tq, Q - q0)
+                kend = K - Q + q0 + qc if causal else K
+                assert all(i["q_count"] == qc for i in its)
+                assert _ranges_tile([(i["t0"], i["t1"]) for i in its], kend)
+    assert not units
+    # partial records: disjoint, inside the float workspace, merged exactly once
+    recs = set()
+    for key, heads in (("decode_items", hpc * g), ("prefill_items", g)):
+        for it in plan[key]:
+            if it["out_rec"] >= 0:
+                span = range(it["out_rec"], it["out_rec"] + it["q_count"] * heads)
+                assert not recs.intersection(span)
+                recs.update(span)
+    assert recs == set(range(info.num_partial_records))
+    merged = set()
+    for m in plan["merges"]:
+        for k in range(m["nslots"]):
+            rec = m["rec_first"] + k * m["rec_stride"]
+            assert rec not in merged
+            merged.add(rec)
+        assert m["nslots"] >= 2
+    assert merged == recs
+    assert info.float_ws_bytes >= info.num_partial_records * (b.head_dim + 1) * 4
+
+
+CONFIGS = {
+    "worked": lambda: W.worked_example(),
+    "decode": lambda: W.batch_decode(with_payload=False),
+    "prefill": lambda: W.append_prefill(with_payload=False),
+    "mixed_p1": lambda: W.mixed_step(page_size=1, with_payload=False),
+    "mixed_p16_hnd": lambda: W.mixed_step(page_size=16, layout="HND", with_payload=False),
+    "ragged": lambda: W.ragged_custom_mask(with_payload=False),
+}
+
+
+def _small_mixed(seed, layout="NHD", page_size=4, ragged=False):
+    rng = np.random.default_rng(seed)
+    n = 9
+    qo = rng.integers(0, 40, size=n)
+    qo[::3] = 1
+    kv = qo + rng.integers(0, 300, size=n)
+    if ragged:
+        b = W.make_ragged_batch(seed, kv, hq=8, hk=2, d=64, mask_mode="custom", with_payload=False)
+        return b
+    return W.make_paged_batch(seed, qo, kv, page_size=page_size, layout=layout, hq=8, hk=2, d=64,
+                              with_payload=False)
+
+
+SMALL = {
+    "worked": lambda: W.worked_example(),
+    "small_p4": lambda: _small_mixed(1),
+    "small_p1_hnd": lambda: _small_mixed(2, "HND", 1),
+    "small_p16": lambda: _small_mixed(3, "NHD", 16),
+    "small_ragged": lambda: _small_mixed(4, ragged=True),
+}
+
+
+def _check_cfg(b, split):
+    params = pka.make_params(b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.layout,
+                             b.mask_mode, kv_ragged=b.kv_ragged, split_mode=split[0],
+                             fixed_split_pages=split[1], num_sms=152)
+    qo = None if b.is_decode else b.qo_indptr
+    plan, info, _ = _dry_plan(params, qo, b.kv_indptr, b.last_page_len)
+    check_coverage(plan, b, b.num_qo_heads, b.num_kv_heads, b.mask_mode == "causal", info)
+    assert info.nnz_qo == b.nnz_q and info.total_kv == int(np.sum(b.kv_lens))
+
+
+@pytest.mark.parametrize("split", [("off", 1), ("auto", 1), ("fixed", 1), ("fixed", 2),
+                                   ("fixed", 7)])
+@pytest.mark.parametrize("cfg", list(SMALL))
+def test_plan_covers_every_key_once_small(cfg, split):
+    _check_cfg(SMALL[cfg](), split)
+
+
+@pytest.mark.parametrize("split", [("off", 1), ("auto", 1), ("fixed", 64)])
+@pytest.mark.parametrize("cfg", list(CONFIGS))
+def test_plan_covers_every_key_once_full_size(cfg, split):
+    if cfg == "ragged" and split[0] == "fixed":
+        split = ("fixed", 2048)  # ragged chunks count tokens
+    _check_cfg(CONFIGS[cfg](), split)
+
+
+def test_auto_split_balances_decode_keys():
+    b = W.batch_decode(with_payload=False)
+    params = pka.make_params(32, 8, 128, 16, num_sms=152)
+    plan, info, _ = _dry_plan(params, None, b.kv_indptr, b.last_page_len)
+    loads = []
+    ptr = plan["decode_cta_ptr"]
+    for c in range(len(ptr) - 1):
+        loads.append(sum(i["t1"] - i["t0"] for i in plan["decode_items"][ptr[c]:ptr[c + 1]]))
+    assert len(loads) <= 153
+    assert max(loads) <= info.decode_chunk_tokens
+    assert sum(loads) == int(np.sum(b.kv_lens))
+
+
+def test_plan_is_deterministic():
+    b = W.mixed_step(page_size=16, layout="HND", with_payload=False)
+    params = pka.make_params(32, 8, 128, 16, "HND", num_sms=152)
+    _, _, a = _dry_plan(params, b.qo_indptr, b.kv_indptr, b.last_page_len)
+    _, _, c = _dry_plan(params, b.qo_indptr, b.kv_indptr, b.last_page_len)
+    assert np.array_equal(a, c)
+
+
+def test_workspace_too_small_reports_sizes():
+    h = pka.pka_plan_create()
+    try:
+        s = pka.pka_plan(h, _p(), *WORKED, None, np.zeros(16, np.uint8), check=False)
+        assert s == WORKSPACE
+        info = pka.pka_plan_get_info(h)
+        assert info.int_ws_bytes > 16
+    finally:
+        pka.pka_plan_destroy(h)
+
+
+def test_stale_plan_detected_before_any_cuda_call():
+    h = pka.pka_plan_create()
+    try:
+        buf = np.zeros(1 << 16, np.uint8)
+        pka.pka_plan(h, _p(), *WORKED, None, buf)
+        lib = _pka.lib()
+        other = _p(page_size=8)
+        import ctypes
+        s = lib.pka_run(h, ctypes.byref(other), 16, 16, 16, 64, 16, None, 16, None, None, 0, None)
+        assert s == STALE
+        same = _p()
+        s = lib.pka_run(h, ctypes.byref(same), 16, 16, 16, 64, 16, None, 16, None, None, 0, None)
+        assert s == INVALID  # a dry-run plan has no device work list
+    finally:
+        pka.pka_plan_destroy(h)
+
+
+def test_null_arguments_rejected():
+    lib = _pka.lib()
+    assert lib.pka_plan_create(None) == INVALID
+    assert lib.pka_packbits(None, 5, None, None) == INVALID
+    assert lib.pka_packbits(None, 0, None, None) == OK
+    assert lib.pka_merge_states(None, None, None, 3, 2, 64, None, None, None) == INVALID
+    assert lib.pka_merge_states(None, None, None, 3, 2, 96, None, None, None) == UNSUPPORTED
+    p = _p()
+    import ctypes
+    assert lib.pka_append_paged_kv_cache(ctypes.byref(p), 3, None, None, None, 5, None, None,
+                                         None, None, None, 64, None) == INVALID

@@ -203,6 +203,11 @@ pka_status pka_merge_states(const float* v, const float* lse, const int32_t* ind
  * the unused high bits of the last byte are 0.  out_d holds (n + 7) / 8 bytes. */
 pka_status pka_packbits(const uint8_t* bools_d, int64_t n, uint8_t* out_d, void* stream);
 
+/* Text of the last CUDA failure behind a PKA_ERR_CUDA returned on the
+ * calling thread (empty if none).  Owned by the library; valid until the
+ * next call on the same thread. */
+const char* pka_last_error(void);
+
 /* Read and clear the device error word written by kernels that gave up on a
  * barrier (0 = none, else a pka_status).  Synchronises `stream`. */
 pka_status pka_get_device_error(int32_t* code, void* stream);

@@ -27,7 +27,7 @@ STATUS = {0: "PKA_OK", 1: "PKA_ERR_INVALID_ARG", 2: "PKA_ERR_METADATA", 3: "PKA_
 EXPORTED = ["pka_status_str", "pka_version", "pka_validate", "pka_plan_create",
             "pka_plan_destroy", "pka_plan", "pka_plan_get_info", "pka_plan_wait", "pka_run",
             "pka_append_paged_kv_cache", "pka_merge_states", "pka_packbits",
-            "pka_get_device_error"]
+            "pka_get_device_error", "pka_last_error"]
 
 
 class pka_params(ctypes.Structure):
@@ -55,7 +55,13 @@ class pka_plan_info(ctypes.Structure):
 class PkaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)} ({_str(status)})")
+        detail = ""
+        if status == 6:
+            try:
+                detail = " — " + lib().pka_last_error().decode()
+            except Exception:
+                pass
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_str(status)}){detail}")
 
 
 _lib = None
@@ -87,8 +93,10 @@ def lib():
         L.pka_merge_states.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.pka_packbits.argtypes = [vp, i64, vp, vp]
         L.pka_get_device_error.argtypes = [P(i32), vp]
+        L.pka_last_error.argtypes = []
+        L.pka_last_error.restype = ctypes.c_char_p
         for name in EXPORTED:
-            if name not in ("pka_status_str", "pka_plan_destroy"):
+            if name not in ("pka_status_str", "pka_plan_destroy", "pka_last_error"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -280,6 +288,10 @@ def pka_merge_states(v, s, indptr, v_out, s_out=None, stream=None):
 def pka_packbits(bools, out, stream=None):
     _check(lib().pka_packbits(_dev(bools, "bools", torch.uint8), bools.numel(),
                               _dev(out, "out", torch.uint8), _stream(stream)), "pka_packbits")
+
+
+def pka_last_error() -> str:
+    return lib().pka_last_error().decode()
 
 
 def pka_get_device_error(stream=None) -> int:

@@ -2,9 +2,9 @@
 //
 // Bandwidth-bound path ("Deep Dive - FlashInfer", "Ragged prefill and paged
 // decode": decode reads a long history per query).  One persistent CTA per
-// SM walks its share of (request, key range) items from the plan.  A
-// producer warp streams 16-key tiles of K and V for all kv heads of the CTA
-// into shared memory with bulk async copies (whole NHD pages or runs of
+// SM walks its share of (request, key range) items from the plan.  Warp 0
+// also acts as producer: it streams 16-key tiles of K and V for all kv heads
+// of the CTA into shared memory with bulk async copies (whole NHD pages or runs of
 // slots, completion counted on an mbarrier); one consumer warp per kv head
 // (two when g = 8) serves that head's g query heads from each tile, so every
 // K/V byte is read from HBM once ("GQA head grouping").  Scores and the online
@@ -98,8 +98,47 @@ __device__ __forceinline__ void issue_tile_copies(const AttnArgs& a, const PkaWo
   }
 }
 
+// Producer cursor over the CTA's (item, 16-key tile) stream.  Warp 0 owns it
+// and keeps `stages` tiles in flight; before refilling a slot it waits until
+// every consumer warp has released it.
+struct Producer {
+  int item;
+  int a0;
+  uint32_t it;
+};
+
+template <int D>
+__device__ __forceinline__ bool produce_one(const AttnArgs& a, Producer& pr, int i1, int stages,
+                                            int hpc, bool head_major, uint16_t* sK, uint16_t* sV,
+                                            int stage_elems, const Bars& bars, int lane,
+                                            volatile int* abort_flag) {
+  while (pr.item < i1) {
+    const PkaWorkItem w = a.items[pr.item];
+    if (pr.a0 < w.t0) pr.a0 = w.t0;
+    if (pr.a0 >= w.t1) {
+      ++pr.item;
+      pr.a0 = -1;
+      continue;
+    }
+    const int s = pr.it % stages;
+    if (!mbar_wait(bars.empty(s), ((pr.it / stages) & 1) ^ 1)) {
+      record_timeout(a.err, abort_flag);
+      return false;
+    }
+    const int n = min(TS, w.t1 - pr.a0);
+    if (lane == 0) mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * n * hpc * D * 2));
+    __syncwarp();
+    issue_tile_copies<D>(a, w, pr.a0, n, hpc, head_major, smem_u32(sK + s * stage_elems),
+                         smem_u32(sV + s * stage_elems), bars.full(s), lane);
+    pr.a0 += TS;
+    ++pr.it;
+    return true;
+  }
+  return false;
+}
+
 template <int D, int GW>
-__global__ void __maxnreg__(224) decode_kernel(const AttnArgs a, const int stages) {
+__global__ void __launch_bounds__(256, 1) decode_kernel(const AttnArgs a, const int stages) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ volatile int abort_flag;
   constexpr int NC = D / 64;  // 64-dim chunks; lane u owns dims c*64 + 8u .. +7
@@ -126,33 +165,15 @@ __global__ void __maxnreg__(224) decode_kernel(const AttnArgs a, const int stage
     fence_mbar_init();
   }
   __syncthreads();
+  if (warp >= n_cons) return;
 
-  if (warp == n_cons) {
-    // ---------------- producer warp ----------------
-    uint32_t it = 0;
-    for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
-      const PkaWorkItem w = a.items[ii];
-      for (int a0 = w.t0; a0 < w.t1; a0 += TS, ++it) {
-        const int s = it % stages;
-        if (!mbar_wait(bars.empty(s), ((it / stages) & 1) ^ 1)) {
-          record_timeout(a.err, &abort_flag);
-          break;
-        }
-        if (abort_flag) break;
-        const int n = min(TS, w.t1 - a0);
-        if (lane == 0) mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * n * hpc * D * 2));
-        __syncwarp();
-        issue_tile_copies<D>(a, w, a0, n, hpc, head_major, smem_u32(sK + s * stage_elems),
-                             smem_u32(sV + s * stage_elems), bars.full(s), lane);
-      }
-    }
-    // Drain: every issued tile's copies must land before the CTA leaves.
-    const uint32_t first = it > (uint32_t)stages ? it - stages : 0;
-    for (uint32_t k = first; k < it; ++k)
-      if (!mbar_wait(bars.full(k % stages), (k / stages) & 1)) record_timeout(a.err, &abort_flag);
-    return;
-  }
-  if (warp > n_cons) return;
+  const bool producer = warp == 0;
+  Producer prod{i0, -1, 0};
+  if (producer)
+    for (int k = 0; k < stages; ++k)
+      if (!produce_one<D>(a, prod, i1, stages, hpc, head_major, sK, sV, stage_elems, bars, lane,
+                          &abort_flag))
+        break;
 
   // ---------------- consumer warps ----------------
   const int hl = warp / wph;     // kv head inside the CTA's block
@@ -296,6 +317,9 @@ __global__ void __maxnreg__(224) decode_kernel(const AttnArgs a, const int stage
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.empty(s));
+      if (producer)
+        produce_one<D>(a, prod, i1, stages, hpc, head_major, sK, sV, stage_elems, bars, lane,
+                       &abort_flag);
     }
     if (abort_flag) break;
 
@@ -348,6 +372,12 @@ __global__ void __maxnreg__(224) decode_kernel(const AttnArgs a, const int stage
       }
     }
   }
+  if (producer) {
+    // Every issued tile's copies must land before the CTA leaves.
+    const uint32_t first = prod.it > (uint32_t)stages ? prod.it - stages : 0;
+    for (uint32_t k = first; k < prod.it; ++k)
+      if (!mbar_wait(bars.full(k % stages), (k / stages) & 1)) record_timeout(a.err, &abort_flag);
+  }
 }
 
 template <int D, int GW>
@@ -362,7 +392,7 @@ cudaError_t launch_t(const AttnArgs& a, int num_ctas, int group, cudaStream_t st
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, GW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, GW><<<num_ctas, 32 * (n_cons + 1), smem, stream>>>(a, stages);
+  decode_kernel<D, GW><<<num_ctas, 32 * n_cons, smem, stream>>>(a, stages);
   return cudaGetLastError();
 }
 

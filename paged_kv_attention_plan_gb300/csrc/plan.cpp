@@ -9,6 +9,7 @@
 // policy here is ours (see split_decode / split_prefill below).
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <functional>
 #include <queue>
@@ -32,6 +33,14 @@ struct pka_plan_s {
 namespace {
 
 constexpr int kMinDecodeChunk = 64;
+
+thread_local char g_last_error[256] = "";
+
+pka_status cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),
+                (int)e);
+  return PKA_ERR_CUDA;
+}
 
 bool params_ok(const pka_params* p) {
   if (!p) return false;
@@ -358,9 +367,9 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   if (num_sms == 0) {
     if (int_ws_d) {
       int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return PKA_ERR_CUDA;
+      cudaError_t e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e, "device query");
     } else {
       num_sms = 152;
     }
@@ -434,14 +443,12 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   plan->int_ws_d = static_cast<int32_t*>(int_ws_d);
   if (int_ws_d) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (!plan->event) {
-      if (cudaEventCreateWithFlags(&plan->event, cudaEventDisableTiming) != cudaSuccess)
-        return PKA_ERR_CUDA;
-    }
-    if (cudaMemcpyAsync(int_ws_d, img, info.int_ws_bytes, cudaMemcpyHostToDevice, st) !=
-        cudaSuccess)
-      return PKA_ERR_CUDA;
-    if (cudaEventRecord(plan->event, st) != cudaSuccess) return PKA_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (!plan->event) e = cudaEventCreateWithFlags(&plan->event, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(int_ws_d, img, info.int_ws_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(plan->event, st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan copy");
     plan->copy_pending = true;
   }
   plan->planned = true;
@@ -509,14 +516,14 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
   if (h.num_decode_items > 0) {
     a.cta_ptr = plan->int_ws_d + h.off_decode_cta_ptr;
     a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_decode_items);
-    if (pka::launch_decode(a, h.num_decode_ctas, p->head_dim, g, st) != cudaSuccess)
-      return PKA_ERR_CUDA;
+    cudaError_t e = pka::launch_decode(a, h.num_decode_ctas, p->head_dim, g, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   if (h.num_prefill_items > 0) {
     a.cta_ptr = plan->int_ws_d + h.off_prefill_cta_ptr;
     a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_prefill_items);
-    if (pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g, st) != cudaSuccess)
-      return PKA_ERR_CUDA;
+    cudaError_t e = pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   if (h.num_merge_tasks > 0) {
     pka::MergeArgs m{};
@@ -528,7 +535,8 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
     m.o = a.o;
     m.lse = lse;
     m.head_dim = p->head_dim;
-    if (pka::launch_merge(m, st) != cudaSuccess) return PKA_ERR_CUDA;
+    cudaError_t e = pka::launch_merge(m, st);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   return PKA_OK;
 }
@@ -545,13 +553,12 @@ pka_status pka_append_paged_kv_cache(const pka_params* p, int32_t batch, const v
   if (!k_new || !v_new || !append_indptr || !kv_indptr || !kv_indices || !last_page_len || !k ||
       !v || page_stride <= 0)
     return PKA_ERR_INVALID_ARG;
-  if (pka::launch_append(*p, batch, static_cast<const uint16_t*>(k_new),
-                         static_cast<const uint16_t*>(v_new), append_indptr, nnz_new, kv_indptr,
-                         kv_indices, last_page_len, static_cast<uint16_t*>(k),
-                         static_cast<uint16_t*>(v), page_stride,
-                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return PKA_ERR_CUDA;
-  return PKA_OK;
+  cudaError_t e = pka::launch_append(*p, batch, static_cast<const uint16_t*>(k_new),
+                                     static_cast<const uint16_t*>(v_new), append_indptr, nnz_new,
+                                     kv_indptr, kv_indices, last_page_len,
+                                     static_cast<uint16_t*>(k), static_cast<uint16_t*>(v),
+                                     page_stride, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : cuda_fail(e, "append launch");
 }
 
 pka_status pka_merge_states(const float* v, const float* lse, const int32_t* indptr,
@@ -570,24 +577,24 @@ pka_status pka_merge_states(const float* v, const float* lse, const int32_t* ind
   m.o = static_cast<uint16_t*>(v_out);
   m.lse = lse_out;
   m.head_dim = dim;
-  return pka::launch_merge(m, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKA_OK
-                                                                                : PKA_ERR_CUDA;
+  cudaError_t e = pka::launch_merge(m, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : cuda_fail(e, "merge launch");
 }
 
 pka_status pka_packbits(const uint8_t* in, int64_t n, uint8_t* out, void* stream) {
   if (n < 0) return PKA_ERR_INVALID_ARG;
   if (n == 0) return PKA_OK;
   if (!in || !out) return PKA_ERR_INVALID_ARG;
-  return pka::launch_packbits(in, n, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PKA_OK
-             : PKA_ERR_CUDA;
+  cudaError_t e = pka::launch_packbits(in, n, out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : cuda_fail(e, "packbits launch");
 }
 
 pka_status pka_get_device_error(int32_t* code, void* stream) {
   if (!code) return PKA_ERR_INVALID_ARG;
-  return pka::read_and_clear_device_error(code, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PKA_OK
-             : PKA_ERR_CUDA;
+  cudaError_t e = pka::read_and_clear_device_error(code, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : cuda_fail(e, "device error read");
 }
+
+const char* pka_last_error(void) { return g_last_error; }
 
 }  // extern "C"

@@ -203,6 +203,31 @@ pka_status pka_merge_states(const float* v, const float* lse, const int32_t* ind
  * the unused high bits of the last byte are 0.  out_d holds (n + 7) / 8 bytes. */
 pka_status pka_packbits(const uint8_t* bools_d, int64_t n, uint8_t* out_d, void* stream);
 
+/* pka_run for callers that cannot allocate device memory when they run
+ * (no cudaMalloc while a stream is captured into a CUDA graph, engines that
+ * give a kernel library no allocator and own every byte of device memory, or
+ * hosts where all allocation happens at start-up).  The paper has no
+ * counterpart to this call.
+ *   Same arguments and results as pka_run, except that the split-KV partial
+ *   states live in a fixed 16 MiB array inside the library's device memory
+ *   (held by every GPU that loads the library until the process exits)
+ *   instead of a caller float workspace.  Allocates nothing: no cudaMalloc,
+ *   cudaFree or allocating library routine.
+ *   A plan whose info.float_ws_bytes exceeds 16 MiB is rejected with
+ *   PKA_ERR_WORKSPACE before anything is launched (pka_last_error says why).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Every call on a device shares the one array and it keeps the last call's
+ *   contents (nothing in it needs to start at zero: each state is written
+ *   before it is read).  Calls whose kernels overlap on the GPU — on two
+ *   streams, or from two threads — race on the array; order them on one
+ *   stream or with events. */
+pka_status pka_run_static_scratch(pka_plan_t plan, const pka_params* params, const void* q,
+                                  const void* k, const void* v, int64_t page_stride,
+                                  const int32_t* kv_indices_d, const uint8_t* packed_mask_d,
+                                  void* o, float* lse, void* stream);
+
 /* Text of the last CUDA failure behind a PKA_ERR_CUDA returned on the
  * calling thread (empty if none).  Owned by the library; valid until the
  * next call on the same thread. */

@@ -14,7 +14,7 @@ from ._pka import (PKA_HND, PKA_MASK_CAUSAL, PKA_MASK_CUSTOM, PKA_MASK_NONE, PKA
                    PKA_SPLIT_AUTO, PKA_SPLIT_FIXED, PKA_SPLIT_OFF, PkaError, make_params,
                    pka_append_paged_kv_cache, pka_get_device_error, pka_last_error, pka_merge_states,
                    pka_packbits, pka_plan, pka_plan_create, pka_plan_destroy, pka_plan_get_info,
-                   pka_plan_wait, pka_run, pka_status_str, pka_validate, pka_version)
+                   pka_plan_wait, pka_run, pka_run_static_scratch, pka_status_str, pka_validate, pka_version)
 
 __all__ = ["BatchAttention", "make_params", "PkaError"] + [n for n in _pka.EXPORTED]
 

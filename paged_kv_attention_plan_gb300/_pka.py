@@ -27,7 +27,7 @@ STATUS = {0: "PKA_OK", 1: "PKA_ERR_INVALID_ARG", 2: "PKA_ERR_METADATA", 3: "PKA_
 EXPORTED = ["pka_status_str", "pka_version", "pka_validate", "pka_plan_create",
             "pka_plan_destroy", "pka_plan", "pka_plan_get_info", "pka_plan_wait", "pka_run",
             "pka_append_paged_kv_cache", "pka_merge_states", "pka_packbits",
-            "pka_get_device_error", "pka_last_error"]
+            "pka_get_device_error", "pka_last_error", "pka_run_static_scratch"]
 
 
 class pka_params(ctypes.Structure):
@@ -88,6 +88,8 @@ def lib():
         L.pka_plan_get_info.argtypes = [vp, P(pka_plan_info)]
         L.pka_plan_wait.argtypes = [vp]
         L.pka_run.argtypes = [vp, P(pka_params), vp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]
+        L.pka_run_static_scratch.argtypes = [vp, P(pka_params), vp, vp, vp, i64, vp, vp, vp, vp,
+                                             vp]
         L.pka_append_paged_kv_cache.argtypes = [P(pka_params), i32, vp, vp, vp, i64, vp, vp, vp,
                                                 vp, vp, i64, vp]
         L.pka_merge_states.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
@@ -258,6 +260,21 @@ def pka_run(handle, params, q, k, v, page_stride, kv_indices, packed_mask, o, ls
                       _dev(lse, "lse", torch.float32), _ptr(float_ws), fws, _stream(stream))
     if check:
         _check(s, "pka_run")
+    return s
+
+
+def pka_run_static_scratch(handle, params, q, k, v, page_stride, kv_indices, packed_mask, o,
+                           lse, stream=None, check=True) -> int:
+    """pka_run with the split-KV scratch in the library's static device array
+    (no workspace from the caller; see include/pka.h)."""
+    bf16 = torch.bfloat16
+    s = lib().pka_run_static_scratch(
+        handle, ctypes.byref(params), _dev(q, "q", bf16), _dev_pool(k, "k"), _dev_pool(v, "v"),
+        int(page_stride), _dev(kv_indices, "kv_indices", torch.int32),
+        _dev(packed_mask, "packed_mask", torch.uint8), _dev(o, "o", bf16),
+        _dev(lse, "lse", torch.float32), _stream(stream))
+    if check:
+        _check(s, "pka_run_static_scratch")
     return s
 
 

@@ -60,6 +60,8 @@ cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
 // Device address of the error word on the current device (null on failure).
 int32_t* device_error_word();
+// Set the text pka_last_error returns on this thread.
+void set_last_error(const char* msg);
 
 // Decode launch geometry shared by the planner and the kernel.
 // A decode CTA covers `heads_per_cta` kv heads; each kv head is served by

@@ -305,6 +305,10 @@ size_t align_words(size_t w) { return (w + 15) & ~size_t(15); }
 
 }  // namespace
 
+void pka::set_last_error(const char* msg) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 extern "C" {
 
 const char* pka_status_str(pka_status s) {

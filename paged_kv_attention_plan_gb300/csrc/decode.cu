@@ -5,9 +5,9 @@
 // SM walks its share of (request, key range) items from the plan.  Warp 0
 // also acts as producer: it streams 16-key tiles of K and V for all kv heads
 // of the CTA into shared memory with bulk async copies (whole NHD pages or runs of
-// slots, completion counted on an mbarrier); one consumer warp per kv head
-// (two when g = 8) serves that head's g query heads from each tile, so every
-// K/V byte is read from HBM once ("GQA head grouping").  Scores and the online
+// slots, completion counted on an mbarrier); the consumer warps of a kv head
+// (one per pair of its g query heads) serve those heads from each tile, so
+// every K/V byte is read from HBM once ("GQA head grouping").  Scores and the online
 // softmax run in fp32 on CUDA cores with packed f32x2 FMAs: eight lanes share
 // one key (16 dims each), four keys per pass.  A CTA writes the final bf16
 // output and base-2 LSE of a request, or, when the plan split the request,
@@ -138,7 +138,7 @@ __device__ __forceinline__ bool produce_one(const AttnArgs& a, Producer& pr, int
 }
 
 template <int D, int GW>
-__global__ void __launch_bounds__(256, 1) decode_kernel(const AttnArgs a, const int stages) {
+__global__ void __launch_bounds__(512, 1) decode_kernel(const AttnArgs a, const int stages) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ volatile int abort_flag;
   constexpr int NC = D / 64;  // 64-dim chunks; lane u owns dims c*64 + 8u .. +7
@@ -402,15 +402,13 @@ cudaError_t launch_decode(const AttnArgs& a0, int num_ctas, int head_dim, int gr
                           cudaStream_t stream) {
   AttnArgs a = a0;
   a.err = device_error_word();
-  const int gw = group < 4 ? group : 4;
+  const int gw = decode_heads_per_warp(group);
   if (head_dim == 128) {
     if (gw == 1) return launch_t<128, 1>(a, num_ctas, group, stream);
-    if (gw == 2) return launch_t<128, 2>(a, num_ctas, group, stream);
-    return launch_t<128, 4>(a, num_ctas, group, stream);
+    return launch_t<128, 2>(a, num_ctas, group, stream);
   }
   if (gw == 1) return launch_t<64, 1>(a, num_ctas, group, stream);
-  if (gw == 2) return launch_t<64, 2>(a, num_ctas, group, stream);
-  return launch_t<64, 4>(a, num_ctas, group, stream);
+  return launch_t<64, 2>(a, num_ctas, group, stream);
 }
 
 }  // namespace pka

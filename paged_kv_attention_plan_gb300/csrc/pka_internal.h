@@ -64,12 +64,16 @@ int32_t* device_error_word();
 void set_last_error(const char* msg);
 
 // Decode launch geometry shared by the planner and the kernel.
-// A decode CTA covers `heads_per_cta` kv heads; each kv head is served by
-// `warps_per_kv_head` consumer warps of up to 4 qo heads each.
-inline int decode_warps_per_kv_head(int group) { return group > 4 ? group / 4 : 1; }
+// A decode CTA covers `heads_per_cta` kv heads (at most 8, so that a 16-key
+// stage of K and V stays within 64 KiB); each kv head is served by
+// `warps_per_kv_head` consumer warps of `decode_heads_per_warp` qo heads each,
+// at most 16 warps per CTA.
+inline int decode_heads_per_warp(int group) { return group < 2 ? group : 2; }
+inline int decode_warps_per_kv_head(int group) { return group / decode_heads_per_warp(group); }
 inline int decode_heads_per_cta(int num_kv_heads, int group) {
   int wph = decode_warps_per_kv_head(group);
-  int h = 8 / wph;
+  int h = 16 / wph;
+  if (h > 8) h = 8;
   if (h > num_kv_heads) h = num_kv_heads;
   while (h > 1 && num_kv_heads % h) --h;
   return h;

@@ -48,8 +48,8 @@ struct MergeArgs {
 
 cudaError_t launch_decode(const AttnArgs& a, int num_ctas, int head_dim, int group,
                           cudaStream_t stream);
-cudaError_t launch_prefill(const AttnArgs& a, int num_ctas, int head_dim, int group,
-                           cudaStream_t stream);
+cudaError_t launch_prefill(const AttnArgs& a, int num_ctas, int head_dim, int group, int nnz_q,
+                           int64_t total_kv, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_packbits(const uint8_t* in, int64_t n, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_new,

@@ -526,7 +526,8 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
   if (h.num_prefill_items > 0) {
     a.cta_ptr = plan->int_ws_d + h.off_prefill_cta_ptr;
     a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_prefill_items);
-    cudaError_t e = pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g, st);
+    cudaError_t e = pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g,
+                                        plan->info.nnz_qo, plan->info.total_kv, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   if (h.num_merge_tasks > 0) {

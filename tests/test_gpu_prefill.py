@@ -1,0 +1,142 @@
+"""GPU parity of the tensor-core append / prefill path (qo_len >= 2 rows).
+
+Covers the worked three-request batch (printed and seeded page ids), the GPU
+smoke-check shape of "Deep Dive - FlashInfer" (32/8 heads, D 128, page size
+4) in bf16, NHD and HND pages of sizes 1..32, head ratios 1/2/4/8, head_dim
+64/128, causal / none / custom masks, ragged K/V, mixed decode + prefill
+batches, every split mode, and the append-prefill and ragged-mask workloads
+at full size (sampled rows against the oracle).
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_attention_plan_gb300 as pka
+from oracle import ref
+from paged_kv_attention_plan_gb300 import workloads as W
+from tests.gpu_util import assert_parity, bf16, f64, i32, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+SPLITS = [("off", 1), ("auto", 1), ("fixed", 1), ("fixed", 2), ("fixed", 7)]
+
+
+@pytest.mark.parametrize("split", SPLITS)
+@pytest.mark.parametrize("literal", [False, True])
+def test_worked_example(split, literal):
+    b = W.worked_example(literal_pages=literal)
+    o, lse, _ = run_gpu(b, split)
+    assert_parity(o, lse, *run_oracle(b))
+
+
+@pytest.mark.parametrize("split", [("auto", 1), ("fixed", 1)])
+def test_smoke_check_shape(split):
+    b = W.worked_example(literal_pages=True, hq=32, hk=8, d=128)
+    o, lse, _ = run_gpu(b, split)
+    assert_parity(o, lse, *run_oracle(b))
+
+
+def _rand_batch(seed, page_size, layout, hq, hk, d, mask="causal", n=5):
+    rng = np.random.default_rng(seed)
+    qo = rng.integers(2, 300, size=n)
+    kv = qo + rng.integers(0, 500, size=n)
+    qo[1] = 2
+    return W.make_paged_batch(seed, qo, kv, page_size=page_size, layout=layout, hq=hq, hk=hk,
+                              d=d, mask_mode=mask)
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("page_size", [1, 4, 16, 32])
+@pytest.mark.parametrize("hq,hk,d", [(32, 8, 128), (8, 8, 64), (16, 8, 128), (16, 2, 64)])
+def test_prefill_shapes(layout, page_size, hq, hk, d):
+    b = _rand_batch(page_size * 7 + hq + d, page_size, layout, hq, hk, d)
+    for split in (("auto", 1), ("fixed", 8)):
+        o, lse, _ = run_gpu(b, split)
+        assert_parity(o, lse, *run_oracle(b))
+
+
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_prefill_mask_modes(mask):
+    b = _rand_batch(91, 16, "NHD", 32, 8, 128, mask=mask)
+    o, lse, _ = run_gpu(b, ("off", 1))
+    assert_parity(o, lse, *run_oracle(b))
+
+
+def test_prefill_custom_mask_paged():
+    b = _rand_batch(92, 16, "NHD", 16, 4, 128, mask="custom")
+    rng = np.random.default_rng(3)
+    bits = []
+    for q, k in zip(b.qo_lens, b.kv_lens):
+        keep = rng.random((q, k)) < 0.5
+        keep[:, -1] = True
+        bits.append(keep.reshape(-1))
+    packed = ref.packbits_little(np.concatenate(bits))
+    for split in (("off", 1), ("fixed", 3)):
+        o, lse, _ = run_gpu(b, split, packed_mask=packed)
+        assert_parity(o, lse, *run_oracle(b, packed_mask=packed))
+
+
+def test_ragged_custom_mask_small():
+    b = W.make_ragged_batch(93, [130, 2, 257, 64], hq=8, hk=8, d=128, mask_mode="custom")
+    packed = ref.packbits_little(b.mask_bool)
+    o, lse, _ = run_gpu(b, ("auto", 1), packed_mask=packed)
+    assert_parity(o, lse, *run_oracle(b, packed_mask=packed))
+
+
+def test_mixed_decode_and_prefill_small():
+    qo = np.array([1, 40, 1, 1, 130, 2, 1], np.int32)
+    kv = np.array([900, 40, 33, 2000, 600, 9, 1], np.int32)
+    for P, layout in ((1, "NHD"), (16, "HND")):
+        b = W.make_paged_batch(94 + P, qo, kv, page_size=P, layout=layout, hq=32, hk=8, d=128)
+        o, lse, info = run_gpu(b, ("auto", 1))
+        assert info.num_decode_items > 0 and info.num_prefill_items > 0
+        assert_parity(o, lse, *run_oracle(b))
+
+
+def _sample_rows(b, per_req=3, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set()
+    for r in range(b.batch_size):
+        q0, q1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
+        if q1 > q0:
+            rows.update({q0, q1 - 1})
+            rows.update(int(x) for x in rng.integers(q0, q1, size=per_req))
+    return rows
+
+
+def test_append_prefill_full_size():
+    """16 requests: append_paged_kv_cache writes the new K/V, then attention."""
+    b = W.append_prefill()
+    params = pka.make_params(32, 8, 128, 16)
+    k, v = bf16(b.k_pool), bf16(b.v_pool)
+    pka.pka_append_paged_kv_cache(params, bf16(b.k_new), bf16(b.v_new), i32(b.qo_indptr),
+                                  i32(b.kv_indptr), i32(b.kv_indices), i32(b.last_page_len), k,
+                                  v, k.stride(0))
+    attn = pka.BatchAttention()
+    attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
+              head_dim=128, page_size=16)
+    o, lse = attn.run(bf16(b.q), k, v, i32(b.kv_indices))
+    torch.cuda.synchronize()
+    assert pka.pka_get_device_error() == 0
+    # the oracle sees the pool with the appended rows written by its own append
+    kr, vr = ref.append_paged_kv_cache(b.k_new, b.v_new, b.qo_indptr, b.k_pool, b.v_pool,
+                                       kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+                                       last_page_len=b.last_page_len, page_size=16)
+    b.k_pool, b.v_pool = kr, vr
+    rows = _sample_rows(b)
+    o_ref, lse_ref = run_oracle(b, rows=rows)
+    assert_parity(f64(o), f64(lse), o_ref, lse_ref, rows=rows)
+
+
+def test_ragged_custom_mask_full_size():
+    b = W.ragged_custom_mask()
+    bools = torch.from_numpy(b.mask_bool).cuda()
+    packed = torch.empty((bools.numel() + 7) // 8, dtype=torch.uint8, device="cuda")
+    pka.pka_packbits(bools, packed)
+    torch.cuda.synchronize()
+    packed_ref = ref.packbits_little(b.mask_bool)
+    assert np.array_equal(packed.cpu().numpy(), packed_ref)
+    o, lse, _ = run_gpu(b, ("auto", 1), packed_mask=packed_ref)
+    rows = _sample_rows(b, per_req=2)
+    o_ref, lse_ref = run_oracle(b, packed_mask=packed_ref, rows=rows)
+    assert_parity(o, lse, o_ref, lse_ref, rows=rows)

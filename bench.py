@@ -184,6 +184,83 @@ def e2e_decode(d, steps, warmup, stream, device):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
+def prefill_flops(b):
+    """Algorithmic FLOPs of attention over visible (query, key) pairs:
+    4 * D * Hq per pair (QK^T and PV, 2 FLOPs per multiply-add)."""
+    pairs = 0
+    for q, k in zip(b.qo_lens, b.kv_lens):
+        q, k = int(q), int(k)
+        if b.mask_mode == "causal":
+            pairs += q * (k - q) + q * (q + 1) // 2
+        else:
+            pairs += q * k
+    return 4 * b.head_dim * b.num_qo_heads * pairs
+
+
+def prefill_setup(device):
+    """Append-prefill workload: append_paged_kv_cache writes the new rows,
+    then causal attention of the new rows against their whole history."""
+    import paged_kv_attention_plan_gb300 as pka
+    from paged_kv_attention_plan_gb300 import workloads as W
+    from tests.gpu_util import bf16, i32
+
+    b = W.append_prefill(seed=1002)
+    d = dict(batch=b, q=bf16(b.q, device), k=bf16(b.k_pool, device), v=bf16(b.v_pool, device),
+             k_new=bf16(b.k_new, device), v_new=bf16(b.v_new, device),
+             idx=i32(b.kv_indices, device), qo=i32(b.qo_indptr, device),
+             kvp=i32(b.kv_indptr, device), last=i32(b.last_page_len, device))
+    d["params"] = pka.make_params(32, 8, 128, 16)
+    attn = pka.BatchAttention(device=device)
+    d["info"] = attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, num_qo_heads=32,
+                          num_kv_heads=8, head_dim=128, page_size=16, split_mode="auto")
+    d["attn"] = attn
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty(b.nnz_q, 32, dtype=torch.float32, device=device)
+    d["flops"] = prefill_flops(b)
+    d["append_bytes"] = 2 * 2 * b.nnz_q * 8 * 128 * 2
+    return d
+
+
+def prefill_append(d):
+    import paged_kv_attention_plan_gb300 as pka
+    pka.pka_append_paged_kv_cache(d["params"], d["k_new"], d["v_new"], d["qo"], d["kvp"], d["idx"],
+                                  d["last"], d["k"], d["v"], d["k"].stride(0))
+
+
+def prefill_attn(d):
+    d["attn"].run(d["q"], d["k"], d["v"], d["idx"], out=d["o"], lse=d["lse"])
+
+
+def ragged_setup(device):
+    """Ragged prefill with a custom mask: packbits of the boolean mask, then
+    attention over ragged K/V (8 requests, 32/32 heads)."""
+    import paged_kv_attention_plan_gb300 as pka
+    from paged_kv_attention_plan_gb300 import workloads as W
+    from tests.gpu_util import bf16
+
+    b = W.ragged_custom_mask(seed=1004)
+    d = dict(batch=b, q=bf16(b.q, device), k=bf16(b.k_pool, device), v=bf16(b.v_pool, device))
+    d["bools"] = torch.from_numpy(b.mask_bool).to(device)
+    d["packed"] = torch.empty((b.mask_bool.size + 7) // 8, dtype=torch.uint8, device=device)
+    attn = pka.BatchAttention(device=device)
+    d["info"] = attn.plan(b.qo_indptr, b.kv_indptr, None, num_qo_heads=32, num_kv_heads=32,
+                          head_dim=128, mask_mode="custom", kv_ragged=True, split_mode="auto")
+    d["attn"] = attn
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty(b.nnz_q, 32, dtype=torch.float32, device=device)
+    d["flops_visible"] = 4 * 128 * 32 * int(b.mask_bool.sum())
+    tiles = sum(((int(n) + 127) // 128) ** 2 for n in b.kv_lens)
+    d["flops_tiles"] = 4 * 128 * 32 * tiles * 128 * 128
+    d["flops_all"] = 4 * 128 * 32 * sum(int(n) ** 2 for n in b.kv_lens)
+    return d
+
+
+def ragged_step(d):
+    import paged_kv_attention_plan_gb300 as pka
+    pka.pka_packbits(d["bools"], d["packed"])
+    d["attn"].run(d["q"], d["k"], d["v"], None, d["packed"], out=d["o"], lse=d["lse"])
+
+
 def oracle_sample(seconds_budget=20.0, max_requests=None):
     """CPU oracle on the first requests of the batch-decode workload."""
     from oracle import ref
@@ -241,6 +318,26 @@ def reference_arm(args, rank):
     print(json.dumps(line))
 
 
+def profile_one(name, device, stream, steps, warmup, pk):
+    """Run one workload's steps only (used under ncu); prints its timings."""
+    if name == "decode":
+        d = decode_setup(device)
+        ms = time_steps(lambda: decode_step(d), steps, warmup, stream)
+        out = {"workload": "batch_decode", "ms": statistics.median(ms),
+               "GB/s": d["bytes"] / (statistics.median(ms) * 1e-3) / 1e9}
+    elif name == "prefill":
+        d = prefill_setup(device)
+        ms = time_steps(lambda: (prefill_append(d), prefill_attn(d)), steps, warmup, stream)
+        out = {"workload": "append_prefill", "ms": statistics.median(ms),
+               "TFLOP/s": d["flops"] / (statistics.median(ms) * 1e-3) / 1e12}
+    else:
+        d = ragged_setup(device)
+        ms = time_steps(lambda: ragged_step(d), steps, warmup, stream)
+        out = {"workload": "ragged_custom_mask", "ms": statistics.median(ms),
+               "TFLOP/s(all pairs)": d["flops_all"] / (statistics.median(ms) * 1e-3) / 1e12}
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -248,6 +345,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "ragged"],
+                    help="all (default) prints the benchmark line; a single workload only runs "
+                         "that workload's kernels (for profiling) and prints its numbers")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -264,8 +364,11 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device(device))
     stream = torch.cuda.current_stream()
 
-    d = decode_setup(device)
     pk = peaks()
+    if args.workload != "all":
+        profile_one(args.workload, device, stream, args.steps, args.warmup, pk)
+        return
+    d = decode_setup(device)
 
     def barrier():
         if world > 1:
@@ -306,6 +409,40 @@ def main():
             "kernel": "decode_kernel<128,4> + merge_kernel<128> (one run())",
             "peak_source": pk["source"]}
 
+    # ---- append + prefill (tensor cores)
+    pf = prefill_setup(device)
+    app_ms = statistics.median(time_steps(lambda: prefill_append(pf), 50, 5, stream))
+    attn_ms = statistics.median(time_steps(lambda: prefill_attn(pf), 50, 5, stream))
+    step_ms = statistics.median(time_steps(lambda: (prefill_append(pf), prefill_attn(pf)), 50, 5,
+                                           stream))
+    attn_tf = pf["flops"] / (attn_ms * 1e-3) / 1e12
+    prefill = {"workload": "append_prefill: 16 req, qo_len U[128,1024], prefix U[0,4096] (seed "
+                           "1002), causal, page 16, 32/8 heads, D 128, bf16 NHD; "
+                           "append_paged_kv_cache then attention",
+               "value": pf["flops"] / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": step_ms, "flops_per_step": pf["flops"],
+               "attn_ms": attn_ms, "append_ms": app_ms,
+               "append_gbs": pf["append_bytes"] / (app_ms * 1e-3) / 1e9,
+               "roofline": {"bound": "tensor", "achieved": attn_tf, "peak": pk["bf16_tflops"],
+                            "unit": "TFLOP/s", "frac": attn_tf / pk["bf16_tflops"],
+                            "frac_of_sustained": attn_tf / pk.get("bf16_tflops_sustained",
+                                                                  pk["bf16_tflops"]),
+                            "traffic": None, "kernel": "prefill_kernel<128>",
+                            "peak_source": pk["source"]},
+               "plan": pf["info"].as_dict()}
+    del pf
+    rg = ragged_setup(device)
+    rg_ms = statistics.median(time_steps(lambda: ragged_step(rg), 50, 5, stream))
+    ragged = {"workload": "ragged_custom_mask: 8 req, qo=kv U[256,2048] (seed 1004), 32/32 "
+                          "heads, D 128, ragged K/V, Bernoulli(0.5) OR causal mask; packbits "
+                          "then attention",
+              "ms_per_step": rg_ms,
+              "tflops_all_pairs": rg["flops_all"] / (rg_ms * 1e-3) / 1e12,
+              "tflops_visible_pairs": rg["flops_visible"] / (rg_ms * 1e-3) / 1e12,
+              "unit": "TFLOP/s"}
+    del rg
+    torch.cuda.empty_cache()
+
     e2e = e2e_decode(d, min(args.steps, 500), 5, stream, device)
     if world > 1:
         import torch.distributed as dist
@@ -323,7 +460,8 @@ def main():
                        "kv_bytes_per_step": d["kv_bytes"], "bytes_per_step": d["bytes"],
                        "l2": "inputs (604 MB of K/V) larger than L2; no flush",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roof, "e2e": e2e, "gpu_launches": d["launches"] * args.steps,
+            "roofline": roof, "prefill": prefill, "ragged_custom_mask": ragged, "e2e": e2e,
+            "gpu_launches": d["launches"] * args.steps,
             "clocks": clocks.summary(), "plan": d["info"].as_dict()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, nreq, secs = oracle_sample(seconds_budget=15.0)

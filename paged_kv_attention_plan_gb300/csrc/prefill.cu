@@ -62,36 +62,54 @@ __device__ __forceinline__ int num_tiles(const PkaWorkItem& w) {
   return w.t1 > w.t0 ? (w.t1 - w.t0 + BN - 1) / BN : 0;
 }
 
-// A page run goes through TMA when it is a whole page of a multiple of 8 rows
-// that lands on a 1024-byte boundary of the tile (the alignment a 128-byte
-// swizzled TMA destination needs); other rows are gathered with 16-byte
-// cp.async into the same swizzled layout.
-__device__ __forceinline__ bool page_by_tma(int P, int pi, int kb, int vend) {
-  return (P % 8) == 0 && P <= BN && pi * P >= kb && pi * P + P <= vend && ((pi * P - kb) % 8) == 0;
+// Split of a tile window [kb, vend) into whole pages loaded by TMA and rows
+// gathered with cp.async.  TMA takes the pages [p_lo, p_hi) that lie fully
+// inside the window when the page size is a multiple of 8 rows (up to 128)
+// and the first of them lands on a 1024-byte boundary of the tile (the
+// alignment of a 128-byte swizzled TMA destination); the rows before and
+// after them ([kb, p_lo*P) and [p_hi*P, vend)) are gathered 16 bytes at a time.
+struct TileSplit {
+  int p_lo, p_hi;   // TMA pages (empty when p_lo >= p_hi)
+  int head_rows;    // cp.async rows at the start of the window
+  int tail_start;   // first cp.async row of the tail (relative to kb)
+  int nrows;        // vend - kb
+};
+
+__device__ __forceinline__ TileSplit split_tile(int P, int kb, int vend) {
+  TileSplit t;
+  t.nrows = vend - kb;
+  t.p_lo = (kb + P - 1) / P;
+  t.p_hi = vend / P;
+  const bool ok = (P % 8) == 0 && P <= BN && t.p_lo < t.p_hi && ((t.p_lo * P - kb) % 8) == 0;
+  if (!ok) {
+    t.p_lo = t.p_hi = 0;
+    t.head_rows = t.nrows;
+    t.tail_start = t.nrows;
+  } else {
+    t.head_rows = t.p_lo * P - kb;
+    t.tail_start = t.p_hi * P - kb;
+  }
+  return t;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// Bytes the TMA part of a tile will deliver (summed over the warp's lanes).
+// Bytes the TMA part of a tile delivers.
 template <int D>
 __device__ __forceinline__ uint32_t kv_tile_tma_bytes(const PrefillParams& pp,
-                                                      const PkaWorkItem& w, int kb, int lane) {
+                                                      const PkaWorkItem& w, int kb) {
   constexpr int NB = D / 64;
   if (pp.a.kv_ragged) return (uint32_t)BN * 128 * NB;
   const int P = pp.a.page_size;
-  const int vend = min(kb + BN, w.kv_len);
-  uint32_t rows = 0;
-  for (int pi = kb / P + lane; pi <= (vend - 1) / P; pi += 32)
-    if (page_by_tma(P, pi, kb, vend)) rows += P;
-  rows = __reduce_add_sync(0xffffffffu, rows);
-  return rows * 128 * NB;
+  const TileSplit t = split_tile(P, kb, min(kb + BN, w.kv_len));
+  return (uint32_t)((t.p_hi - t.p_lo) * P) * 128 * NB;
 }
 
 // Issue the loads of one 128-key tile of K (or V) for kv head w.kv_head0:
 // rows [kb, vend) of the window; rows past vend keep older finite data and
-// are masked.  Lanes share the pages of the window.
+// are masked.  Lanes share the pages and rows of the window.
 template <int D>
 __device__ __forceinline__ void load_kv_tile(const PrefillParams& pp, const CUtensorMap* map,
                                              const uint16_t* pool, const PkaWorkItem& w, int kb,
@@ -107,11 +125,9 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& pp, const CUte
   }
   const int P = a.page_size;
   const int Hk = a.num_kv_heads;
-  const int vend = min(kb + BN, w.kv_len);
+  const TileSplit t = split_tile(P, kb, min(kb + BN, w.kv_len));
   const bool nhd = a.layout == PKA_NHD;
-  // whole aligned pages: one TMA box per 64-dim block
-  for (int pi = kb / P + lane; pi <= (vend - 1) / P; pi += 32) {
-    if (!page_by_tma(P, pi, kb, vend)) continue;
+  for (int pi = t.p_lo + lane; pi < t.p_hi; pi += 32) {
     const int page = a.kv_indices[w.kv_base + pi];
     const uint32_t d = dst + (uint32_t)(pi * P - kb) * 128;
 #pragma unroll
@@ -122,14 +138,14 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& pp, const CUte
         tc::tma_load_4d(d + c * BLK, map, c * 64, 0, w.kv_head0, page, bar);
     }
   }
-  // every other row: 16-byte chunks, swizzled by hand (chunk ^ (row & 7))
+  // gathered rows: 16-byte chunks, swizzled by hand (chunk ^ (row & 7))
   constexpr int CH = D / 8;  // 16-byte chunks per row
-  const int nrows = vend - kb;
-  for (int x = lane; x < nrows * CH; x += 32) {
-    const int r = x / CH, ch = x % CH;
+  const int gathered = t.head_rows + (t.nrows - t.tail_start);
+  for (int x = lane; x < gathered * CH; x += 32) {
+    const int q = x / CH, ch = x - q * CH;
+    const int r = q < t.head_rows ? q : t.tail_start + (q - t.head_rows);
     const int j = kb + r;
     const int pi = j / P;
-    if (page_by_tma(P, pi, kb, vend)) continue;
     const int page = a.kv_indices[w.kv_base + pi];
     const int slot = j - pi * P;
     const int64_t off = (int64_t)page * a.page_stride +
@@ -252,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int kb = w.t0 + k * BN;
-        const uint32_t bytes = kv_tile_tma_bytes<D>(pp, w, kb, lane);
+        const uint32_t bytes = kv_tile_tma_bytes<D>(pp, w, kb);
         if (lane == 0) {
           mbar_arrive_expect_tx(smem_u32(&bars.k_full[s]), bytes);
           mbar_arrive_expect_tx(smem_u32(&bars.v_full[s]), bytes);
@@ -373,28 +389,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_sync();
-        float x[BN];
+        float x[BN];  // raw scores q.k (scaled below inside the exponent)
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tc::tmem_ld32(tS + (t & 1) * BN + lane_off + c * 32, r);
-          tc::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(r[j]) * a.scale_log2;
+          for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(r[j]);
         }
+        tc::tmem_ld_wait();
         const int kb = w.t0 + k * BN;
         int vis_end = w.t1 - kb;  // columns >= vis_end are outside the key range
         if (a.mask_mode == PKA_MASK_CAUSAL) vis_end = min(vis_end, klim - kb + 1);
         uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
         if (a.mask_mode == PKA_MASK_CUSTOM)
           load_mask_bits(a.mask, mrow + kb, mrow + min(w.t1, w.kv_len), mbits);
-        float mx = -INFINITY;
+        float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int j = 0; j < BN; ++j) {
           const bool vis = j < vis_end && ((mbits[j >> 5] >> (j & 31)) & 1u);
           x[j] = vis ? x[j] : -INFINITY;
-          mx = fmaxf(mx, x[j]);
+          mxa[j & 3] = fmaxf(mxa[j & 3], x[j]);
         }
+        // row max in log2 units (scale > 0 keeps the order)
+        const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])) * a.scale_log2;
         float alpha = 1.f;
         if (m == -INFINITY) {
           m = mx;
@@ -403,15 +421,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mx;
         }
         const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
-        float sum = 0.f;
+        float suma[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[BN / 2];
+        if (m == -INFINITY) {
 #pragma unroll
-        for (int j = 0; j < BN; j += 2) {
-          const float p0 = m == -INFINITY ? 0.f : exp2f(x[j] - m);
-          const float p1 = m == -INFINITY ? 0.f : exp2f(x[j + 1] - m);
-          sum += p0 + p1;
-          pk[j / 2] = float2_to_bf16x2(p0, p1);
+          for (int j = 0; j < BN / 2; ++j) pk[j] = 0u;
+        } else {
+          const float neg_m = -m;
+#pragma unroll
+          for (int j = 0; j < BN; j += 2) {
+            const float p0 = exp2f(fmaf(x[j], a.scale_log2, neg_m));
+            const float p1 = exp2f(fmaf(x[j + 1], a.scale_log2, neg_m));
+            suma[(j >> 1) & 3] += p0 + p1;
+            pk[j / 2] = float2_to_bf16x2(p0, p1);
+          }
         }
+        const float sum = (suma[0] + suma[1]) + (suma[2] + suma[3]);
         l = l * alpha + sum;
         // P and O may only change once the previous P V product has finished.
         if (k >= 1) {

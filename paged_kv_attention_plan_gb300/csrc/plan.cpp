@@ -232,13 +232,13 @@ void plan_decode(const pka_params* p, const Batch& b, int num_sms, PlanLists* L)
 }
 
 // Rows of requests with qo_len >= 2 go to the tensor-core kernel: units are
-// (request, kv head, tile of 128 / g query tokens) so that the g qo heads of
-// one kv head pack into a 128-row tile and share every K/V load.  Causal
+// (request, kv head, 2 x 128 / g query tokens): the g qo heads of one kv head
+// pack with the tokens into two 128-row tiles that share every K/V load.  Causal
 // units only visit keys up to the tile's last visible one.  Items are dealt
 // to CTAs longest-first onto the least loaded CTA.
 void plan_prefill(const pka_params* p, const Batch& b, int num_sms, PlanLists* L) {
   int g = p->num_qo_heads / p->num_kv_heads;
-  int tq = pka::kPrefillTileRows / g;
+  int tq = 2 * (pka::kPrefillTileRows / g);
   struct Unit { int r, h, q0, qc, kend; };
   std::vector<Unit> units;
   int64_t total_tiles = 0;

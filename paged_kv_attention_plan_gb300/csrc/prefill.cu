@@ -32,7 +32,7 @@ constexpr int BM = kPrefillTileRows;  // 128 packed rows
 constexpr int BN = kPrefillTileKeys;  // 128 keys
 constexpr int STAGES = 2;
 constexpr uint32_t BLK = 16384;       // one [128 rows x 128 B] swizzled block
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // softmax warpgroups 0-1, producer warp 8, MMA warp 9
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 struct Maps {
@@ -49,8 +49,7 @@ struct PrefillParams {
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
-  uint64_t s_full[2];
-  uint64_t p_full, o_done, o_free;
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];  // per query tile
 };
 
 __device__ __forceinline__ void fail(const AttnArgs& a, volatile int* abort_flag) {
@@ -192,10 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ = smem;                              // NB blocks
-  uint8_t* sK = sQ + NB * BLK;                     // STAGES x NB blocks
-  uint8_t* sV = sK + STAGES * NB * BLK;            // STAGES x NB blocks
-  uint8_t* sP = sV + STAGES * NB * BLK;            // 2 blocks (128 keys)
+  uint8_t* sQ = smem;                    // 2 tiles x NB blocks
+  uint8_t* sK = sQ + 2 * NB * BLK;       // STAGES x NB blocks
+  uint8_t* sV = sK + STAGES * NB * BLK;  // STAGES x NB blocks
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -203,8 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i0 = a.cta_ptr[blockIdx.x], i1 = a.cta_ptr[blockIdx.x + 1];
   const int G = pp.group;
+  const int TQ = BM / G;  // query tokens of one 128-row tile
 
-  // Zero the K/V stages once: rows of a partial tile that no TMA writes must
+  // Zero the K/V stages once: rows of a partial tile that no load writes must
   // hold finite values (P is 0 there, and 0 * NaN would poison O).
   for (int x = threadIdx.x; x < 2 * STAGES * NB * (int)BLK / 16; x += kThreads)
     reinterpret_cast<uint4*>(sK)[x] = make_uint4(0, 0, 0, 0);
@@ -217,15 +216,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.v_full[s]), 33);
       mbar_init(smem_u32(&bars.kv_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bars.s_full[0]), 1);
-    mbar_init(smem_u32(&bars.s_full[1]), 1);
-    mbar_init(smem_u32(&bars.p_full), BM);
-    mbar_init(smem_u32(&bars.o_done), 1);
-    mbar_init(smem_u32(&bars.o_free), BM);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&bars.s_full[x]), 1);
+      mbar_init(smem_u32(&bars.p_full[x]), BM);
+      mbar_init(smem_u32(&bars.o_done[x]), 1);
+      mbar_init(smem_u32(&bars.o_free[x]), BM);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tc::tmem_alloc(smem_u32(&tmem_base_sh), 512);
     tc::tmem_relinquish();
   }
@@ -233,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tS = tmem;            // two S buffers: columns [0,128) and [128,256)
-  const uint32_t tO = tmem + 256;      // O: columns [256, 256 + D)
+  // TMEM columns: S of tile x at [128x, 128x + 128) (P, bf16, reuses its first
+  // 64 columns), O of tile x at [256 + 128x, 256 + 128x + D).
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tc::prefetch_tmap(&maps.q);
@@ -248,16 +248,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const PkaWorkItem w = a.items[ii];
       const int n = num_tiles(w);
       if (n == 0) continue;
+      const bool two = w.q_count > TQ;
       if (q_uses > 0 && !mbar_wait(smem_u32(&bars.q_empty), (q_uses - 1) & 1)) {
         fail(a, &abort_flag);
         break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(smem_u32(&bars.q_full), NB * BLK);
+        mbar_arrive_expect_tx(smem_u32(&bars.q_full), (two ? 2 : 1) * NB * BLK);
+        for (int x = 0; x < (two ? 2 : 1); ++x)
 #pragma unroll
-        for (int c = 0; c < NB; ++c)
-          tc::tma_load_3d(smem_u32(sQ + c * BLK), &maps.q, c * 64, w.kv_head0 * G, w.q_row0,
-                          smem_u32(&bars.q_full));
+          for (int c = 0; c < NB; ++c)
+            tc::tma_load_3d(smem_u32(sQ + (x * NB + c) * BLK), &maps.q, c * 64, w.kv_head0 * G,
+                            w.q_row0 + x * TQ, smem_u32(&bars.q_full));
       }
       ++q_uses;
       for (int k = 0; k < n; ++k, ++kv_it) {
@@ -294,125 +296,142 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail(a, &abort_flag);
     }
     if (q_uses > 0 && !mbar_wait(smem_u32(&bars.q_full), (q_uses - 1) & 1)) fail(a, &abort_flag);
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Order per key tile k (two query tiles A and B):
+    //   PV_A(k), S_A(k+1), PV_B(k), S_B(k+1)
+    // so that the tensor core works on one tile while the other tile's
+    // softmax runs.  MMAs of one thread execute in issue order, so S_x(k+1)
+    // may overwrite the P_x(k) that PV_x(k) reads.
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(BM, D, false, true);
-      uint32_t kv_it = 0, gt = 0, q_uses = 0, o_uses = 0;
-      auto pv = [&](uint32_t tile_kv_it, uint32_t tile_gt, bool first) -> bool {
-        const int s = tile_kv_it % STAGES;
-        if (!mbar_wait(smem_u32(&bars.p_full), tile_gt & 1)) return false;
-        if (!mbar_wait(smem_u32(&bars.v_full[s]), (tile_kv_it / STAGES) & 1)) return false;
-        tc::fence_after_sync();
+      uint32_t kv_it = 0, q_uses = 0;
+      uint32_t uses[2] = {0, 0}, o_uses[2] = {0, 0};
+      bool ok = true;
+      auto issue_s = [&](int x, uint32_t it) {
+        const int s = it % STAGES;
+        const uint32_t qb = smem_u32(sQ + x * NB * BLK);
+        const uint32_t kbase = smem_u32(sK + s * NB * BLK);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = tc::smem_desc_sw128(qb + (kk / 4) * BLK + (kk % 4) * 32, 16, 1024);
+          const uint64_t bd =
+              tc::smem_desc_sw128(kbase + (kk / 4) * BLK + (kk % 4) * 32, 16, 1024);
+          tc::mma_bf16(tmem + x * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(smem_u32(&bars.s_full[x]));
+      };
+      auto issue_pv = [&](int x, uint32_t it, bool first) {
+        const int s = it % STAGES;
         const uint32_t vb = smem_u32(sV + s * NB * BLK);
-        const uint32_t pb = smem_u32(sP);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t ad = tc::smem_desc_sw128(pb + (kk / 4) * BLK + (kk % 4) * 32, 16, 1024);
           const uint64_t bd = tc::smem_desc_sw128(vb + kk * 2048, BLK, 1024);
-          tc::mma_bf16(tO, ad, bd, idO, (first && kk == 0) ? 0u : 1u);
+          tc::mma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, bd, idO,
+                          (first && kk == 0) ? 0u : 1u);
         }
-        tc::mma_commit(smem_u32(&bars.o_done));
-        tc::mma_commit(smem_u32(&bars.kv_empty[s]));
-        return true;
+        tc::mma_commit(smem_u32(&bars.o_done[x]));
       };
-      for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
+      for (int ii = i0; ii < i1 && ok && !abort_flag; ++ii) {
         const PkaWorkItem w = a.items[ii];
         const int n = num_tiles(w);
         if (n == 0) continue;
-        if (!mbar_wait(smem_u32(&bars.q_full), q_uses & 1)) {
-          fail(a, &abort_flag);
-          break;
-        }
+        const int nx = w.q_count > TQ ? 2 : 1;
+        ok = mbar_wait(smem_u32(&bars.q_full), q_uses & 1);
         ++q_uses;
+        if (ok) ok = mbar_wait(smem_u32(&bars.k_full[kv_it % STAGES]), (kv_it / STAGES) & 1);
+        if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t qb = smem_u32(sQ);
-        bool ok = true;
+        for (int x = 0; x < nx; ++x) issue_s(x, kv_it);
         for (int k = 0; k < n && ok; ++k) {
           const uint32_t it = kv_it + k;
-          const int s = it % STAGES;
-          if (!mbar_wait(smem_u32(&bars.k_full[s]), (it / STAGES) & 1)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t kbase = smem_u32(sK + s * NB * BLK);
-          const uint32_t dS = tS + ((gt + k) & 1) * BN;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = tc::smem_desc_sw128(qb + (kk / 4) * BLK + (kk % 4) * 32, 16, 1024);
-            const uint64_t bd = tc::smem_desc_sw128(kbase + (kk / 4) * BLK + (kk % 4) * 32, 16, 1024);
-            tc::mma_bf16(dS, ad, bd, idS, kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(smem_u32(&bars.s_full[(gt + k) & 1]));
-          if (k >= 1) {
-            if (k == 1 && o_uses > 0 && !mbar_wait(smem_u32(&bars.o_free), (o_uses - 1) & 1)) {
-              ok = false;
-              break;
+          for (int x = 0; x < nx && ok; ++x) {
+            ok = mbar_wait(smem_u32(&bars.p_full[x]), (uses[x] + k) & 1);
+            if (ok && k == 0 && o_uses[x] > 0)
+              ok = mbar_wait(smem_u32(&bars.o_free[x]), (o_uses[x] - 1) & 1);
+            if (ok && x == 0)
+              ok = mbar_wait(smem_u32(&bars.v_full[it % STAGES]), (it / STAGES) & 1);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_pv(x, it, k == 0);
+            if (k + 1 < n) {
+              if (x == 0) {
+                ok = mbar_wait(smem_u32(&bars.k_full[(it + 1) % STAGES]), ((it + 1) / STAGES) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+              }
+              issue_s(x, it + 1);
             }
-            ok = pv(it - 1, gt + k - 1, k == 1);
           }
+          tc::mma_commit(smem_u32(&bars.kv_empty[it % STAGES]));
         }
         tc::mma_commit(smem_u32(&bars.q_empty));
-        if (ok && n == 1 && o_uses > 0 && !mbar_wait(smem_u32(&bars.o_free), (o_uses - 1) & 1))
-          ok = false;
-        if (ok) ok = pv(kv_it + n - 1, gt + n - 1, n == 1);
-        if (!ok) {
-          fail(a, &abort_flag);
-          break;
+        for (int x = 0; x < nx; ++x) {
+          uses[x] += n;
+          o_uses[x] += 1;
         }
         kv_it += n;
-        gt += n;
-        ++o_uses;
       }
+      if (!ok) fail(a, &abort_flag);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int row = threadIdx.x;             // 0..127 == TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int i_tok = row / G, g = row % G;
-    uint32_t gt = 0;
+    const int x = warp >> 2;                 // query tile of this warpgroup
+    const int row = threadIdx.x & (BM - 1);  // TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + x * 128 + lane_off;
+    const int i_tok = x * TQ + row / G, g = row % G;
+    const float sc = a.scale_log2;
+    uint32_t uses = 0;
     for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
       const PkaWorkItem w = a.items[ii];
+      if (x == 1 && w.q_count <= TQ) continue;  // no second tile in this item
       const int n = num_tiles(w);
       const int i = w.q_local0 + i_tok;              // query index inside the request
       const int klim = w.kv_len - w.qo_len + i;      // causal: keys <= klim are visible
+      const int klim_first = w.kv_len - w.qo_len + w.q_local0 + x * TQ;
       const int64_t mrow = ((int64_t)w.mask_hi << 32 | (uint32_t)w.mask_lo) + (int64_t)i * w.kv_len;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int k = 0; k < n; ++k) {
-        const uint32_t t = gt + k;
-        if (!mbar_wait(smem_u32(&bars.s_full[t & 1]), (t >> 1) & 1)) {
+        if (!mbar_wait(smem_u32(&bars.s_full[x]), (uses + k) & 1)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        float x[BN];  // raw scores q.k (scaled below inside the exponent)
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(tS + (t & 1) * BN + lane_off + c * 32, r);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(r[j]);
-        }
-        tc::tmem_ld_wait();
         const int kb = w.t0 + k * BN;
-        int vis_end = w.t1 - kb;  // columns >= vis_end are outside the key range
+        // Only tiles that reach past the key range, the causal diagonal of the
+        // warpgroup's first row, or a custom mask need per-element masking.
+        const bool need_mask = (kb + BN > w.t1) || a.mask_mode == PKA_MASK_CUSTOM ||
+                               (a.mask_mode == PKA_MASK_CAUSAL && kb + BN - 1 > klim_first);
+        int vis_end = w.t1 - kb;
         if (a.mask_mode == PKA_MASK_CAUSAL) vis_end = min(vis_end, klim - kb + 1);
         uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
         if (a.mask_mode == PKA_MASK_CUSTOM)
           load_mask_bits(a.mask, mrow + kb, mrow + min(w.t1, w.kv_len), mbits);
+        // pass 1: row max
         float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          const bool vis = j < vis_end && ((mbits[j >> 5] >> (j & 31)) & 1u);
-          x[j] = vis ? x[j] : -INFINITY;
-          mxa[j & 3] = fmaxf(mxa[j & 3], x[j]);
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld32(tS + c * 32, r);
+          tc::tmem_ld_wait();
+          if (need_mask) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int col = c * 32 + j;
+              const bool vis = col < vis_end && ((mbits[c] >> j) & 1u);
+              mxa[j & 3] = fmaxf(mxa[j & 3], vis ? __uint_as_float(r[j]) : -INFINITY);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mxa[j & 3] = fmaxf(mxa[j & 3], __uint_as_float(r[j]));
+          }
         }
-        // row max in log2 units (scale > 0 keeps the order)
-        const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])) * a.scale_log2;
+        const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])) * sc;
         float alpha = 1.f;
         if (m == -INFINITY) {
           m = mx;
@@ -420,68 +439,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = exp2f(m - mx);
           m = mx;
         }
-        const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+        // pass 2: probabilities -> P (bf16) over the first 64 columns of S
         float suma[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[BN / 2];
-        if (m == -INFINITY) {
+        const float neg_m = m == -INFINITY ? 0.f : -m;
+        const bool none = m == -INFINITY;
 #pragma unroll
-          for (int j = 0; j < BN / 2; ++j) pk[j] = 0u;
-        } else {
-          const float neg_m = -m;
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld32(tS + c * 32, r);
+          tc::tmem_ld_wait();
+          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < BN; j += 2) {
-            const float p0 = exp2f(fmaf(x[j], a.scale_log2, neg_m));
-            const float p1 = exp2f(fmaf(x[j + 1], a.scale_log2, neg_m));
+          for (int j = 0; j < 32; j += 2) {
+            float p0 = exp2f(fmaf(__uint_as_float(r[j]), sc, neg_m));
+            float p1 = exp2f(fmaf(__uint_as_float(r[j + 1]), sc, neg_m));
+            if (need_mask) {
+              const int col = c * 32 + j;
+              if (!(col < vis_end && ((mbits[c] >> j) & 1u))) p0 = 0.f;
+              if (!(col + 1 < vis_end && ((mbits[c] >> (j + 1)) & 1u))) p1 = 0.f;
+            }
+            if (none) p0 = p1 = 0.f;
             suma[(j >> 1) & 3] += p0 + p1;
             pk[j / 2] = float2_to_bf16x2(p0, p1);
           }
+          tc::tmem_st16(tS + c * 16, pk);
         }
-        const float sum = (suma[0] + suma[1]) + (suma[2] + suma[3]);
-        l = l * alpha + sum;
-        // P and O may only change once the previous P V product has finished.
-        if (k >= 1) {
-          if (!mbar_wait(smem_u32(&bars.o_done), (t - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          if (rescale) {
+        l = l * alpha + ((suma[0] + suma[1]) + (suma[2] + suma[3]));
+        // O of the earlier key tiles is final here: S_x(k) was issued after
+        // PV_x(k-1), and MMAs complete in order.
+        if (k >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tc::tmem_ld32(tO + lane_off + c * 32, r);
-              tc::tmem_ld_wait();
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tc::tmem_ld32(tO + c * 32, r);
+            tc::tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-              tc::tmem_st32(tO + lane_off + c * 32, r);
-            }
-            tc::tmem_st_wait();
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+            tc::tmem_st32(tO + c * 32, r);
           }
         }
-        // P row -> shared memory, 128-byte swizzled K-major layout
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t off = blk * BLK + row * 128 + ((ch ^ (row & 7)) * 16);
-            *reinterpret_cast<uint4*>(sP + off) =
-                make_uint4(pk[blk * 32 + ch * 4 + 0], pk[blk * 32 + ch * 4 + 1],
-                           pk[blk * 32 + ch * 4 + 2], pk[blk * 32 + ch * 4 + 3]);
-          }
-        tc::fence_proxy_async_smem();
+        tc::tmem_st_wait();
         tc::fence_before_sync();
-        mbar_arrive(smem_u32(&bars.p_full));
+        mbar_arrive(smem_u32(&bars.p_full[x]));
       }
       if (!ok) {
         fail(a, &abort_flag);
         break;
       }
       // ---------------- epilogue
-      float o[D];
-#pragma unroll
-      for (int j = 0; j < D; ++j) o[j] = 0.f;
+      const bool store = i_tok < w.q_count;
+      const bool any = l > 0.f;
+      const float inv = any ? 1.f / l : 0.f;
+      const int head = w.kv_head0 * G + g;
+      uint16_t* odst = a.o + ((int64_t)(w.q_row0 + i_tok) * a.num_qo_heads + head) * D;
+      const int rec = w.out_rec + i_tok * G + g;
+      float* pdst = a.part_o + (int64_t)rec * D;
       if (n > 0) {
-        if (!mbar_wait(smem_u32(&bars.o_done), (gt + n - 1) & 1)) {
+        if (!mbar_wait(smem_u32(&bars.o_done[x]), (uses + n - 1) & 1)) {
           fail(a, &abort_flag);
           break;
         }
@@ -489,46 +503,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
-          tc::tmem_ld32(tO + lane_off + c * 32, r);
+          tc::tmem_ld32(tO + c * 32, r);
           tc::tmem_ld_wait();
+          if (!store) continue;
+          if (w.out_rec < 0) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[c * 32 + j] = __uint_as_float(r[j]);
+            for (int j = 0; j < 32; j += 8) {
+              uint4 v;
+              v.x = float2_to_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
+              v.y = float2_to_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+              v.z = float2_to_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
+              v.w = float2_to_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
+              *reinterpret_cast<uint4*>(odst + c * 32 + j) = v;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(pdst + c * 32 + j) =
+                  make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
+                              __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+          }
         }
         tc::fence_before_sync();
-        mbar_arrive(smem_u32(&bars.o_free));
-      }
-      gt += n;
-      if (i_tok >= w.q_count) continue;
-      const bool any = l > 0.f;
-      const float inv = any ? 1.f / l : 0.f;
-      const float lse_v = any ? m + log2f(l) : -INFINITY;
-      const int head = w.kv_head0 * G + g;
-      if (w.out_rec < 0) {
-        uint16_t* dst = a.o + ((int64_t)(w.q_row0 + i_tok) * a.num_qo_heads + head) * D;
-#pragma unroll
+        mbar_arrive(smem_u32(&bars.o_free[x]));
+      } else if (store) {
+        // empty key range: zero output
         for (int j = 0; j < D; j += 8) {
-          uint4 v;
-          v.x = float2_to_bf16x2(o[j] * inv, o[j + 1] * inv);
-          v.y = float2_to_bf16x2(o[j + 2] * inv, o[j + 3] * inv);
-          v.z = float2_to_bf16x2(o[j + 4] * inv, o[j + 5] * inv);
-          v.w = float2_to_bf16x2(o[j + 6] * inv, o[j + 7] * inv);
-          *reinterpret_cast<uint4*>(dst + j) = v;
+          if (w.out_rec < 0)
+            *reinterpret_cast<uint4*>(odst + j) = make_uint4(0, 0, 0, 0);
+          else {
+            *reinterpret_cast<float4*>(pdst + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(pdst + j + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
+      }
+      uses += n;
+      if (!store) continue;
+      const float lse_v = any ? m + log2f(l) : -INFINITY;
+      if (w.out_rec < 0) {
         if (a.lse) a.lse[(int64_t)(w.q_row0 + i_tok) * a.num_qo_heads + head] = lse_v;
       } else {
-        const int rec = w.out_rec + i_tok * G + g;
-        float* dst = a.part_o + (int64_t)rec * D;
-#pragma unroll
-        for (int j = 0; j < D; j += 4)
-          *reinterpret_cast<float4*>(dst + j) =
-              make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
         a.part_lse[rec] = lse_v;
       }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
@@ -610,7 +631,7 @@ cudaError_t launch_t(const PrefillParams& pp, int num_ctas, int nnz_q, int64_t t
   }
   constexpr int NB = D / 64;
   // At least 120 KiB, so that one CTA (and its 512 TMEM columns) owns each SM.
-  size_t smem = 1024 + (size_t)(NB + 2 * STAGES * NB + 2) * BLK;
+  size_t smem = 1024 + (size_t)(2 * NB + 2 * STAGES * NB) * BLK;
   if (smem < 120 * 1024) smem = 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

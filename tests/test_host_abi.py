@@ -135,7 +135,7 @@ def check_coverage(plan, b, hq, hk, causal, info):
             assert _ranges_tile([(i["t0"], i["t1"]) for i in its], int(kv_len[r]))
             assert all(i["q_row0"] == b.qo_indptr[r] for i in its)
     assert not units
-    tq = 128 // g
+    tq = 256 // g  # two 128-row tiles of packed (token, head) rows per item
     for it in plan["prefill_items"]:
         assert qo_len[it["req"]] >= 2 and it["n_kv_heads"] == 1
         units.setdefault((it["req"], it["kv_head0"], it["q_local0"]), []).append(it)

@@ -5,9 +5,12 @@
 
 namespace pka {
 
-// A wait that polls this many times without success gives up, records
-// PKA_ERR_DEVICE_TIMEOUT in the device error word and lets the CTA leave.
-constexpr uint32_t kSpinLimit = 1u << 24;
+// A barrier wait suspends the warp (up to kSuspendNs per poll) until the
+// phase completes; after kWaitPolls polls (a few seconds) it gives up, the
+// caller records PKA_ERR_DEVICE_TIMEOUT in the device error word and the CTA
+// leaves.
+constexpr uint32_t kSuspendNs = 1000000;  // 1 ms
+constexpr uint32_t kWaitPolls = 4000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -43,10 +46,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the completion of the phase with the given parity.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
   return false;
 }
 

@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = tc::idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(BM, D, false, true);
       uint32_t kv_it = 0, q_uses = 0;
-      uint32_t uses[2] = {0, 0}, o_uses[2] = {0, 0};
+      uint32_t uses0 = 0, uses1 = 0, o_uses0 = 0, o_uses1 = 0;  // per query tile
       bool ok = true;
       auto issue_s = [&](int x, uint32_t it) {
         const int s = it % STAGES;
@@ -347,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < n && ok; ++k) {
           const uint32_t it = kv_it + k;
           for (int x = 0; x < nx && ok; ++x) {
-            ok = mbar_wait(smem_u32(&bars.p_full[x]), (uses[x] + k) & 1);
-            if (ok && k == 0 && o_uses[x] > 0)
-              ok = mbar_wait(smem_u32(&bars.o_free[x]), (o_uses[x] - 1) & 1);
+            const uint32_t ux = x ? uses1 : uses0, ox = x ? o_uses1 : o_uses0;
+            ok = mbar_wait(smem_u32(&bars.p_full[x]), (ux + k) & 1);
+            if (ok && k == 0 && ox > 0) ok = mbar_wait(smem_u32(&bars.o_free[x]), (ox - 1) & 1);
             if (ok && x == 0)
               ok = mbar_wait(smem_u32(&bars.v_full[it % STAGES]), (it / STAGES) & 1);
             if (!ok) break;
@@ -367,9 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_commit(smem_u32(&bars.kv_empty[it % STAGES]));
         }
         tc::mma_commit(smem_u32(&bars.q_empty));
-        for (int x = 0; x < nx; ++x) {
-          uses[x] += n;
-          o_uses[x] += 1;
+        uses0 += n;
+        o_uses0 += 1;
+        if (nx == 2) {
+          uses1 += n;
+          o_uses1 += 1;
         }
         kv_it += n;
       }
@@ -412,23 +414,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
         if (a.mask_mode == PKA_MASK_CUSTOM)
           load_mask_bits(a.mask, mrow + kb, mrow + min(w.t1, w.kv_len), mbits);
-        // pass 1: row max
+        // pass 1: row max; the load of chunk c+1 is in flight while chunk c
+        // is reduced
         float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(tS + c * 32, r);
+        {
+          uint32_t rb[2][32];
+          tc::tmem_ld32(tS, rb[0]);
           tc::tmem_ld_wait();
-          if (need_mask) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = c * 32 + j;
-              const bool vis = col < vis_end && ((mbits[c] >> j) & 1u);
-              mxa[j & 3] = fmaxf(mxa[j & 3], vis ? __uint_as_float(r[j]) : -INFINITY);
+          for (int c = 0; c < BN / 32; ++c) {
+            if (c + 1 < BN / 32) tc::tmem_ld32(tS + (c + 1) * 32, rb[(c + 1) & 1]);
+            const uint32_t (&r)[32] = rb[c & 1];
+            if (need_mask) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int col = c * 32 + j;
+                const bool vis = col < vis_end && ((mbits[c] >> j) & 1u);
+                mxa[j & 3] = fmaxf(mxa[j & 3], vis ? __uint_as_float(r[j]) : -INFINITY);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) mxa[j & 3] = fmaxf(mxa[j & 3], __uint_as_float(r[j]));
             }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mxa[j & 3] = fmaxf(mxa[j & 3], __uint_as_float(r[j]));
+            if (c + 1 < BN / 32) tc::tmem_ld_wait();
           }
         }
         const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])) * sc;
@@ -439,15 +447,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = exp2f(m - mx);
           m = mx;
         }
-        // pass 2: probabilities -> P (bf16) over the first 64 columns of S
+        // pass 2: probabilities -> P (bf16) over the first 64 columns of S.
+        // The load of chunk c+1 is in flight while chunk c is computed.
         float suma[4] = {0.f, 0.f, 0.f, 0.f};
         const float neg_m = m == -INFINITY ? 0.f : -m;
         const bool none = m == -INFINITY;
+        uint32_t rb[2][32];
+        tc::tmem_ld32(tS, rb[0]);
+        tc::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(tS + c * 32, r);
-          tc::tmem_ld_wait();
+          if (c + 1 < BN / 32) tc::tmem_ld32(tS + (c + 1) * 32, rb[(c + 1) & 1]);
+          const uint32_t (&r)[32] = rb[c & 1];
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
@@ -463,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[j / 2] = float2_to_bf16x2(p0, p1);
           }
           tc::tmem_st16(tS + c * 16, pk);
+          if (c + 1 < BN / 32) tc::tmem_ld_wait();
         }
         l = l * alpha + ((suma[0] + suma[1]) + (suma[2] + suma[3]));
         // O of the earlier key tiles is final here: S_x(k) was issued after

@@ -13,10 +13,13 @@
 // writes bf16 O and the base-2 LSE, or a normalised fp32 partial state that
 // the merge kernel combines ("A worked split-KV example").
 //
-// Warp roles (192 threads): warps 0-3 softmax and epilogue (thread = row =
-// TMEM lane), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer.
-// S is double-buffered in TMEM so that QK^T of tile k+1 overlaps the softmax
-// of tile k; K/V tiles use a two-stage ring.
+// Warp roles (320 threads): warpgroups 0 and 1 run the softmax and epilogue
+// of two 128-row query tiles of the same (request, kv head) (thread = row =
+// TMEM lane); warp 8 is the TMA / cp.async producer, warp 9 allocates TMEM and
+// issues the MMAs.  Both query tiles share each K/V tile (two-stage ring) and
+// the tensor core alternates between them, so one tile's MMAs overlap the
+// other tile's softmax.  P stays in tensor memory (it overwrites the first
+// half of its S tile) and feeds the P V product as the A operand.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -51,6 +54,20 @@ struct Bars {
   uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];  // per query tile
 };
+
+// 2^x on the special-function unit (inputs here are <= 8; results below the
+// smallest normal flush to 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 __device__ __forceinline__ void fail(const AttnArgs& a, volatile int* abort_flag) {
   *abort_flag = 1;
@@ -427,14 +444,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t (&r)[32] = rb[c & 1];
             if (need_mask) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
+              for (int j = 0; j < 32; j += 2) {
                 const int col = c * 32 + j;
-                const bool vis = col < vis_end && ((mbits[c] >> j) & 1u);
-                mxa[j & 3] = fmaxf(mxa[j & 3], vis ? __uint_as_float(r[j]) : -INFINITY);
+                const bool v0 = col < vis_end && ((mbits[c] >> j) & 1u);
+                const bool v1 = col + 1 < vis_end && ((mbits[c] >> (j + 1)) & 1u);
+                mxa[(j >> 1) & 3] = max3(mxa[(j >> 1) & 3], v0 ? __uint_as_float(r[j]) : -INFINITY,
+                                         v1 ? __uint_as_float(r[j + 1]) : -INFINITY);
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) mxa[j & 3] = fmaxf(mxa[j & 3], __uint_as_float(r[j]));
+              for (int j = 0; j < 32; j += 2)
+                mxa[(j >> 1) & 3] =
+                    max3(mxa[(j >> 1) & 3], __uint_as_float(r[j]), __uint_as_float(r[j + 1]));
             }
             if (c + 1 < BN / 32) tc::tmem_ld_wait();
           }
@@ -449,8 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // pass 2: probabilities -> P (bf16) over the first 64 columns of S.
         // The load of chunk c+1 is in flight while chunk c is computed.
-        float suma[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         const float neg_m = m == -INFINITY ? 0.f : -m;
+        const float2 sc2 = make_float2(sc, sc), negm2 = make_float2(neg_m, neg_m);
         const bool none = m == -INFINITY;
         uint32_t rb[2][32];
         tc::tmem_ld32(tS, rb[0]);
@@ -462,21 +484,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            float p0 = exp2f(fmaf(__uint_as_float(r[j]), sc, neg_m));
-            float p1 = exp2f(fmaf(__uint_as_float(r[j + 1]), sc, neg_m));
+            const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                         sc2, negm2);
+            float p0 = ex2(t2.x);
+            float p1 = ex2(t2.y);
             if (need_mask) {
               const int col = c * 32 + j;
               if (!(col < vis_end && ((mbits[c] >> j) & 1u))) p0 = 0.f;
               if (!(col + 1 < vis_end && ((mbits[c] >> (j + 1)) & 1u))) p1 = 0.f;
             }
             if (none) p0 = p1 = 0.f;
-            suma[(j >> 1) & 3] += p0 + p1;
+            sum2[(j >> 1) & 1] = __fadd2_rn(sum2[(j >> 1) & 1], make_float2(p0, p1));
             pk[j / 2] = float2_to_bf16x2(p0, p1);
           }
           tc::tmem_st16(tS + c * 16, pk);
           if (c + 1 < BN / 32) tc::tmem_ld_wait();
         }
-        l = l * alpha + ((suma[0] + suma[1]) + (suma[2] + suma[3]));
+        l = l * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
         // O of the earlier key tiles is final here: S_x(k) was issued after
         // PV_x(k-1), and MMAs complete in order.
         if (k >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {

@@ -13,12 +13,12 @@
 // writes bf16 O and the base-2 LSE, or a normalised fp32 partial state that
 // the merge kernel combines ("A worked split-KV example").
 //
-// Warp roles (320 threads): warpgroups 0 and 1 run the softmax and epilogue
+// Warp roles (352 threads): warpgroups 0 and 1 run the softmax and epilogue
 // of two 128-row query tiles of the same (request, kv head) (thread = row =
-// TMEM lane); warp 8 is the TMA / cp.async producer, warp 9 allocates TMEM and
-// issues the MMAs.  Both query tiles share each K/V tile (two-stage ring) and
-// the tensor core alternates between them, so one tile's MMAs overlap the
-// other tile's softmax.  P stays in tensor memory (it overwrites the first
+// TMEM lane); warp 8 loads Q and the K ring, warp 10 the V ring (TMA for
+// whole pages, cp.async for the rest), warp 9 allocates TMEM and issues the
+// MMAs.  Both query tiles share each K/V tile and the tensor core alternates
+// between them, so one tile's MMAs overlap the other tile's softmax.  P stays in tensor memory (it overwrites the first
 // half of its S tile) and feeds the P V product as the A operand.
 #include <cudaTypedefs.h>
 
@@ -33,9 +33,15 @@ namespace {
 
 constexpr int BM = kPrefillTileRows;  // 128 packed rows
 constexpr int BN = kPrefillTileKeys;  // 128 keys
-constexpr int STAGES = 2;
+// K tiles are released as soon as both QK^T products have read them, V tiles
+// only after both P V products, so the K ring runs deeper than the V ring.
+template <int D> struct Ring {
+  static constexpr int K = D == 128 ? 3 : 4;
+  static constexpr int V = D == 128 ? 2 : 4;
+};
 constexpr uint32_t BLK = 16384;       // one [128 rows x 128 B] swizzled block
-constexpr int kThreads = 320;  // softmax warpgroups 0-1, producer warp 8, MMA warp 9
+// softmax warpgroups 0-1, Q+K producer warp 8, MMA warp 9, V producer warp 10
+constexpr int kThreads = 352;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 struct Maps {
@@ -51,7 +57,7 @@ struct PrefillParams {
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[STAGES], v_full[STAGES], kv_empty[STAGES];
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];  // per query tile
 };
 
@@ -208,9 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ = smem;                    // 2 tiles x NB blocks
-  uint8_t* sK = sQ + 2 * NB * BLK;       // STAGES x NB blocks
-  uint8_t* sV = sK + STAGES * NB * BLK;  // STAGES x NB blocks
+  constexpr int KS = Ring<D>::K, VS = Ring<D>::V;
+  uint8_t* sQ = smem;                // 2 tiles x NB blocks
+  uint8_t* sK = sQ + 2 * NB * BLK;   // KS x NB blocks
+  uint8_t* sV = sK + KS * NB * BLK;  // VS x NB blocks
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -222,16 +229,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Zero the K/V stages once: rows of a partial tile that no load writes must
   // hold finite values (P is 0 there, and 0 * NaN would poison O).
-  for (int x = threadIdx.x; x < 2 * STAGES * NB * (int)BLK / 16; x += kThreads)
+  for (int x = threadIdx.x; x < (KS + VS) * NB * (int)BLK / 16; x += kThreads)
     reinterpret_cast<uint4*>(sK)[x] = make_uint4(0, 0, 0, 0);
   tc::fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars.q_full), 1);
     mbar_init(smem_u32(&bars.q_empty), 1);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(smem_u32(&bars.k_full[s]), 33);  // TMA expect_tx + 32 producer lanes
+      mbar_init(smem_u32(&bars.k_empty[s]), 1);
+    }
+    for (int s = 0; s < VS; ++s) {
       mbar_init(smem_u32(&bars.v_full[s]), 33);
-      mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+      mbar_init(smem_u32(&bars.v_empty[s]), 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&bars.s_full[x]), 1);
@@ -253,66 +263,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM columns: S of tile x at [128x, 128x + 128) (P, bf16, reuses its first
   // 64 columns), O of tile x at [256 + 128x, 256 + 128x + D).
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // warp 8: Q tiles and the K ring; warp 10: the V ring.
+    const bool kq = warp == 8;
+    const int ns = kq ? KS : VS;
+    uint64_t* full = kq ? bars.k_full : bars.v_full;
+    uint64_t* empty = kq ? bars.k_empty : bars.v_empty;
+    uint8_t* ring = kq ? sK : sV;
+    const CUtensorMap* map = kq ? &maps.kv_k : &maps.kv_v;
+    const uint16_t* pool = kq ? a.k : a.v;
     if (lane == 0) {
-      tc::prefetch_tmap(&maps.q);
-      tc::prefetch_tmap(&maps.kv_k);
-      tc::prefetch_tmap(&maps.kv_v);
+      if (kq) tc::prefetch_tmap(&maps.q);
+      tc::prefetch_tmap(map);
     }
-    uint32_t kv_it = 0, q_uses = 0;
+    uint32_t it = 0, q_uses = 0;
     for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
       const PkaWorkItem w = a.items[ii];
       const int n = num_tiles(w);
       if (n == 0) continue;
-      const bool two = w.q_count > TQ;
-      if (q_uses > 0 && !mbar_wait(smem_u32(&bars.q_empty), (q_uses - 1) & 1)) {
-        fail(a, &abort_flag);
-        break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(smem_u32(&bars.q_full), (two ? 2 : 1) * NB * BLK);
-        for (int x = 0; x < (two ? 2 : 1); ++x)
+      if (kq) {
+        const bool two = w.q_count > TQ;
+        if (q_uses > 0 && !mbar_wait(smem_u32(&bars.q_empty), (q_uses - 1) & 1)) {
+          fail(a, &abort_flag);
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(smem_u32(&bars.q_full), (two ? 2 : 1) * NB * BLK);
+          for (int x = 0; x < (two ? 2 : 1); ++x)
 #pragma unroll
-          for (int c = 0; c < NB; ++c)
-            tc::tma_load_3d(smem_u32(sQ + (x * NB + c) * BLK), &maps.q, c * 64, w.kv_head0 * G,
-                            w.q_row0 + x * TQ, smem_u32(&bars.q_full));
+            for (int c = 0; c < NB; ++c)
+              tc::tma_load_3d(smem_u32(sQ + (x * NB + c) * BLK), &maps.q, c * 64, w.kv_head0 * G,
+                              w.q_row0 + x * TQ, smem_u32(&bars.q_full));
+        }
+        ++q_uses;
       }
-      ++q_uses;
-      for (int k = 0; k < n; ++k, ++kv_it) {
-        const int s = kv_it % STAGES;
-        if (kv_it >= STAGES &&
-            !mbar_wait(smem_u32(&bars.kv_empty[s]), ((kv_it / STAGES) - 1) & 1)) {
+      for (int k = 0; k < n; ++k, ++it) {
+        const int s = it % ns;
+        if (it >= (uint32_t)ns && !mbar_wait(smem_u32(&empty[s]), ((it / ns) - 1) & 1)) {
           fail(a, &abort_flag);
           break;
         }
         const int kb = w.t0 + k * BN;
         const uint32_t bytes = kv_tile_tma_bytes<D>(pp, w, kb);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(smem_u32(&bars.k_full[s]), bytes);
-          mbar_arrive_expect_tx(smem_u32(&bars.v_full[s]), bytes);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), bytes);
         __syncwarp();
-        load_kv_tile<D>(pp, &maps.kv_k, a.k, w, kb, smem_u32(sK + s * NB * BLK),
-                        smem_u32(&bars.k_full[s]), lane);
-        load_kv_tile<D>(pp, &maps.kv_v, a.v, w, kb, smem_u32(sV + s * NB * BLK),
-                        smem_u32(&bars.v_full[s]), lane);
+        load_kv_tile<D>(pp, map, pool, w, kb, smem_u32(ring + s * NB * BLK), smem_u32(&full[s]),
+                        lane);
         // Gathered rows are generic-proxy writes: wait for this lane's copies,
         // make them visible to the tensor cores, then arrive.
         asm volatile("cp.async.wait_all;" ::: "memory");
         tc::fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&bars.k_full[s]));
-        mbar_arrive(smem_u32(&bars.v_full[s]));
+        mbar_arrive(smem_u32(&full[s]));
       }
     }
     // Drain: the loads of the last stages must land before the CTA leaves.
-    for (uint32_t k = kv_it > STAGES ? kv_it - STAGES : 0; k < kv_it; ++k) {
-      const int s = k % STAGES;
-      if (!mbar_wait(smem_u32(&bars.k_full[s]), (k / STAGES) & 1) ||
-          !mbar_wait(smem_u32(&bars.v_full[s]), (k / STAGES) & 1))
-        fail(a, &abort_flag);
-    }
-    if (q_uses > 0 && !mbar_wait(smem_u32(&bars.q_full), (q_uses - 1) & 1)) fail(a, &abort_flag);
+    for (uint32_t k = it > (uint32_t)ns ? it - ns : 0; k < it; ++k)
+      if (!mbar_wait(smem_u32(&full[k % ns]), (k / ns) & 1)) fail(a, &abort_flag);
+    if (kq && q_uses > 0 && !mbar_wait(smem_u32(&bars.q_full), (q_uses - 1) & 1))
+      fail(a, &abort_flag);
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // Order per key tile k (two query tiles A and B):
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t uses0 = 0, uses1 = 0, o_uses0 = 0, o_uses1 = 0;  // per query tile
       bool ok = true;
       auto issue_s = [&](int x, uint32_t it) {
-        const int s = it % STAGES;
+        const int s = it % KS;
         const uint32_t qb = smem_u32(sQ + x * NB * BLK);
         const uint32_t kbase = smem_u32(sK + s * NB * BLK);
 #pragma unroll
@@ -340,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(smem_u32(&bars.s_full[x]));
       };
       auto issue_pv = [&](int x, uint32_t it, bool first) {
-        const int s = it % STAGES;
+        const int s = it % VS;
         const uint32_t vb = smem_u32(sV + s * NB * BLK);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
@@ -357,31 +366,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nx = w.q_count > TQ ? 2 : 1;
         ok = mbar_wait(smem_u32(&bars.q_full), q_uses & 1);
         ++q_uses;
-        if (ok) ok = mbar_wait(smem_u32(&bars.k_full[kv_it % STAGES]), (kv_it / STAGES) & 1);
+        if (ok) ok = mbar_wait(smem_u32(&bars.k_full[kv_it % KS]), (kv_it / KS) & 1);
         if (!ok) break;
         tc::fence_after_sync();
         for (int x = 0; x < nx; ++x) issue_s(x, kv_it);
+        tc::mma_commit(smem_u32(&bars.k_empty[kv_it % KS]));
         for (int k = 0; k < n && ok; ++k) {
           const uint32_t it = kv_it + k;
           for (int x = 0; x < nx && ok; ++x) {
             const uint32_t ux = x ? uses1 : uses0, ox = x ? o_uses1 : o_uses0;
             ok = mbar_wait(smem_u32(&bars.p_full[x]), (ux + k) & 1);
             if (ok && k == 0 && ox > 0) ok = mbar_wait(smem_u32(&bars.o_free[x]), (ox - 1) & 1);
-            if (ok && x == 0)
-              ok = mbar_wait(smem_u32(&bars.v_full[it % STAGES]), (it / STAGES) & 1);
+            if (ok && x == 0) ok = mbar_wait(smem_u32(&bars.v_full[it % VS]), (it / VS) & 1);
             if (!ok) break;
             tc::fence_after_sync();
             issue_pv(x, it, k == 0);
             if (k + 1 < n) {
               if (x == 0) {
-                ok = mbar_wait(smem_u32(&bars.k_full[(it + 1) % STAGES]), ((it + 1) / STAGES) & 1);
+                ok = mbar_wait(smem_u32(&bars.k_full[(it + 1) % KS]), ((it + 1) / KS) & 1);
                 if (!ok) break;
                 tc::fence_after_sync();
               }
               issue_s(x, it + 1);
+              if (x == nx - 1) tc::mma_commit(smem_u32(&bars.k_empty[(it + 1) % KS]));
             }
           }
-          tc::mma_commit(smem_u32(&bars.kv_empty[it % STAGES]));
+          tc::mma_commit(smem_u32(&bars.v_empty[it % VS]));
         }
         tc::mma_commit(smem_u32(&bars.q_empty));
         uses0 += n;
@@ -667,7 +677,7 @@ cudaError_t launch_t(const PrefillParams& pp, int num_ctas, int nnz_q, int64_t t
   }
   constexpr int NB = D / 64;
   // At least 120 KiB, so that one CTA (and its 512 TMEM columns) owns each SM.
-  size_t smem = 1024 + (size_t)(2 * NB + 2 * STAGES * NB) * BLK;
+  size_t smem = 1024 + (size_t)(2 + Ring<D>::K + Ring<D>::V) * NB * BLK;
   if (smem < 120 * 1024) smem = 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

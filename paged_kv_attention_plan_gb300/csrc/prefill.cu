@@ -335,28 +335,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kv_it = 0, q_uses = 0;
       uint32_t uses0 = 0, uses1 = 0, o_uses0 = 0, o_uses1 = 0;  // per query tile
       bool ok = true;
+      // Descriptor bases are built once; each MMA only adds the (constant)
+      // start-address offset of its 16-wide K slice, in 16-byte units.
+      const uint64_t dq0 = tc::smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(sV), BLK, 1024);
       auto issue_s = [&](int x, uint32_t it) {
-        const int s = it % KS;
-        const uint32_t qb = smem_u32(sQ + x * NB * BLK);
-        const uint32_t kbase = smem_u32(sK + s * NB * BLK);
+        const uint64_t ad = dq0 + (uint64_t)((x * NB * BLK) >> 4);
+        const uint64_t bd = dk0 + (uint64_t)(((it % KS) * NB * BLK) >> 4);
+        const uint32_t d = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = tc::smem_desc_sw128(qb + (kk / 4) * BLK + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd =
-              tc::smem_desc_sw128(kbase + (kk / 4) * BLK + (kk % 4) * 32, 16, 1024);
-          tc::mma_bf16(tmem + x * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk / 4) * BLK + (kk % 4) * 32) >> 4);
+          tc::mma_bf16(d, ad + off, bd + off, idS, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(smem_u32(&bars.s_full[x]));
       };
       auto issue_pv = [&](int x, uint32_t it, bool first) {
-        const int s = it % VS;
-        const uint32_t vb = smem_u32(sV + s * NB * BLK);
+        const uint64_t bd = dv0 + (uint64_t)(((it % VS) * NB * BLK) >> 4);
+        const uint32_t d = tmem + 256 + x * 128, pa = tmem + x * 128;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = tc::smem_desc_sw128(vb + kk * 2048, BLK, 1024);
-          tc::mma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, bd, idO,
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc::mma_bf16_ts(d, pa + kk * 8, bd + (uint64_t)((kk * 2048) >> 4), idO,
                           (first && kk == 0) ? 0u : 1u);
-        }
         tc::mma_commit(smem_u32(&bars.o_done[x]));
       };
       for (int ii = i0; ii < i1 && ok && !abort_flag; ++ii) {
@@ -441,35 +442,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
         if (a.mask_mode == PKA_MASK_CUSTOM)
           load_mask_bits(a.mask, mrow + kb, mrow + min(w.t1, w.kv_len), mbits);
-        // pass 1: row max; the load of chunk c+1 is in flight while chunk c
-        // is reduced
-        float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        {
-          uint32_t rb[2][32];
-          tc::tmem_ld32(tS, rb[0]);
-          tc::tmem_ld_wait();
+        // The whole S row in one round trip (four 32-column loads, one wait):
+        // under tensor-core traffic a TMEM load takes hundreds of cycles, so
+        // one exposed latency per tile instead of one per chunk.
+        uint32_t r[BN / 32][32];
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
-            if (c + 1 < BN / 32) tc::tmem_ld32(tS + (c + 1) * 32, rb[(c + 1) & 1]);
-            const uint32_t (&r)[32] = rb[c & 1];
-            if (need_mask) {
+        for (int c = 0; c < BN / 32; ++c) tc::tmem_ld32(tS + c * 32, r[c]);
+        tc::tmem_ld_wait();
+        if (need_mask) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 2) {
-                const int col = c * 32 + j;
-                const bool v0 = col < vis_end && ((mbits[c] >> j) & 1u);
-                const bool v1 = col + 1 < vis_end && ((mbits[c] >> (j + 1)) & 1u);
-                mxa[(j >> 1) & 3] = max3(mxa[(j >> 1) & 3], v0 ? __uint_as_float(r[j]) : -INFINITY,
-                                         v1 ? __uint_as_float(r[j + 1]) : -INFINITY);
-              }
-            } else {
+          for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-              for (int j = 0; j < 32; j += 2)
-                mxa[(j >> 1) & 3] =
-                    max3(mxa[(j >> 1) & 3], __uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+            for (int j = 0; j < 32; ++j) {
+              const int col = c * 32 + j;
+              if (!(col < vis_end && ((mbits[c] >> j) & 1u))) r[c][j] = __float_as_uint(-INFINITY);
             }
-            if (c + 1 < BN / 32) tc::tmem_ld_wait();
-          }
         }
+        float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; j += 2)
+            mxa[(j >> 1) & 3] =
+                max3(mxa[(j >> 1) & 3], __uint_as_float(r[c][j]), __uint_as_float(r[c][j + 1]));
         const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])) * sc;
         float alpha = 1.f;
         if (m == -INFINITY) {
@@ -478,37 +473,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = exp2f(m - mx);
           m = mx;
         }
-        // pass 2: probabilities -> P (bf16) over the first 64 columns of S.
-        // The load of chunk c+1 is in flight while chunk c is computed.
+        // probabilities (masked scores are -inf and give 0) -> P, bf16, packed
+        // in place over the consumed scores and stored over the first 64
+        // columns of S
         float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        const float neg_m = m == -INFINITY ? 0.f : -m;
-        const float2 sc2 = make_float2(sc, sc), negm2 = make_float2(neg_m, neg_m);
         const bool none = m == -INFINITY;
-        uint32_t rb[2][32];
-        tc::tmem_ld32(tS, rb[0]);
-        tc::tmem_ld_wait();
+        const float neg_m = none ? 0.f : -m;
+        const float2 sc2 = make_float2(sc, sc), negm2 = make_float2(neg_m, neg_m);
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
-          if (c + 1 < BN / 32) tc::tmem_ld32(tS + (c + 1) * 32, rb[(c + 1) & 1]);
-          const uint32_t (&r)[32] = rb[c & 1];
-          uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                         sc2, negm2);
+            const float2 t2 = __ffma2_rn(
+                make_float2(__uint_as_float(r[c][j]), __uint_as_float(r[c][j + 1])), sc2, negm2);
             float p0 = ex2(t2.x);
             float p1 = ex2(t2.y);
-            if (need_mask) {
-              const int col = c * 32 + j;
-              if (!(col < vis_end && ((mbits[c] >> j) & 1u))) p0 = 0.f;
-              if (!(col + 1 < vis_end && ((mbits[c] >> (j + 1)) & 1u))) p1 = 0.f;
-            }
             if (none) p0 = p1 = 0.f;
             sum2[(j >> 1) & 1] = __fadd2_rn(sum2[(j >> 1) & 1], make_float2(p0, p1));
-            pk[j / 2] = float2_to_bf16x2(p0, p1);
+            r[c][j / 2] = float2_to_bf16x2(p0, p1);
           }
-          tc::tmem_st16(tS + c * 16, pk);
-          if (c + 1 < BN / 32) tc::tmem_ld_wait();
+          tc::tmem_st16(tS + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&r[c][0]));
         }
         l = l * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
         // O of the earlier key tiles is final here: S_x(k) was issued after

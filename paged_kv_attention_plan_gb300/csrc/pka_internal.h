@@ -63,18 +63,13 @@ int32_t* device_error_word();
 // Set the text pka_last_error returns on this thread.
 void set_last_error(const char* msg);
 
-// Decode launch geometry shared by the planner and the kernel.
-// A decode CTA covers `heads_per_cta` kv heads (at most 8, so that a 16-key
-// stage of K and V stays within 64 KiB); each kv head is served by
-// `warps_per_kv_head` consumer warps of `decode_heads_per_warp` qo heads each,
-// at most 16 warps per CTA.
-inline int decode_heads_per_warp(int group) { return group < 2 ? group : 2; }
-inline int decode_warps_per_kv_head(int group) { return group / decode_heads_per_warp(group); }
+// Decode launch geometry shared by the planner and the kernel: a decode CTA
+// covers `heads_per_cta` kv heads (at most 8, one consumer warp each, so that
+// a 16-key stage of K and V stays near 64 KiB); each warp serves all g <= 8
+// qo heads of its kv head.
 inline int decode_heads_per_cta(int num_kv_heads, int group) {
-  int wph = decode_warps_per_kv_head(group);
-  int h = 16 / wph;
-  if (h > 8) h = 8;
-  if (h > num_kv_heads) h = num_kv_heads;
+  (void)group;
+  int h = num_kv_heads < 8 ? num_kv_heads : 8;
   while (h > 1 && num_kv_heads % h) --h;
   return h;
 }

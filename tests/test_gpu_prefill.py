@@ -140,3 +140,44 @@ def test_ragged_custom_mask_full_size():
     rows = _sample_rows(b, per_req=2)
     o_ref, lse_ref = run_oracle(b, packed_mask=packed_ref, rows=rows)
     assert_parity(o, lse, o_ref, lse_ref, rows=rows)
+
+
+@pytest.mark.parametrize("page_size,layout", [(1, "NHD"), (16, "HND")])
+def test_mixed_step_full_size(page_size, layout):
+    """8 long decodes (32K-131K keys), 120 short decodes and 4 prefill chunks of
+    512 tokens in one plan; decode rows and prefill rows sampled."""
+    from paged_kv_attention_plan_gb300 import workloads as Wk
+    b = Wk.mixed_step(page_size=page_size, layout=layout, with_payload=False)
+    rng = np.random.default_rng(5)
+    # payload drawn on the host only for the pages the sampled rows read
+    hk, d = 8, 128
+    pool = int(b.extra["pool_pages"])
+    shape = (pool, page_size, hk, d) if layout == "NHD" else (pool, hk, page_size, d)
+    g = torch.Generator(device="cuda").manual_seed(1003)
+    k = torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn((b.nnz_q, 32, d), generator=g, device="cuda").to(torch.bfloat16)
+    attn = pka.BatchAttention()
+    info = attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
+                     head_dim=128, page_size=page_size, layout=layout)
+    assert info.num_decode_items > 0 and info.num_prefill_items > 0 and info.num_merge_tasks > 0
+    o, lse = attn.run(q, k, v, i32(b.kv_indices))
+    torch.cuda.synchronize()
+    assert pka.pka_get_device_error() == 0
+    # sampled rows: 2 long decodes, 3 short decodes, first/last rows of 2 chunks
+    reqs = [0, 7, 8, 60, 127, 128, 131]
+    rows = set()
+    for r in reqs:
+        q0, q1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
+        rows.update({q0, q1 - 1})
+    # copy only the pages of the sampled requests to the host
+    b.q = q.view(torch.int16).cpu().numpy().view(np.uint16)
+    page_ids = np.concatenate([b.kv_indices[b.kv_indptr[r]:b.kv_indptr[r + 1]] for r in reqs])
+    kh = np.zeros(shape, np.uint16)
+    vh = np.zeros(shape, np.uint16)
+    idx = torch.from_numpy(page_ids.astype(np.int64)).cuda()
+    kh[page_ids] = k.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+    vh[page_ids] = v.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+    b.k_pool, b.v_pool = kh, vh
+    o_ref, lse_ref = run_oracle(b, rows=rows)
+    assert_parity(f64(o), f64(lse), o_ref, lse_ref, rows=rows)

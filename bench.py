@@ -261,6 +261,41 @@ def ragged_step(d):
     d["attn"].run(d["q"], d["k"], d["v"], None, d["packed"], out=d["o"], lse=d["lse"])
 
 
+def mixed_setup(device, page_size, layout):
+    """Mixed serving step: 8 long + 120 short decodes and 4 prefill chunks of
+    512 tokens in one plan (decode kernel, tensor-core kernel, merge)."""
+    import paged_kv_attention_plan_gb300 as pka
+    from paged_kv_attention_plan_gb300 import workloads as W
+    from tests.gpu_util import i32
+
+    b = W.mixed_step(seed=1003, page_size=page_size, layout=layout, with_payload=False)
+    pool = int(b.extra["pool_pages"])
+    shape = (pool, page_size, 8, 128) if layout == "NHD" else (pool, 8, page_size, 128)
+    g = torch.Generator(device=device).manual_seed(1003)
+    d = dict(batch=b)
+    d["k"] = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    d["v"] = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+    d["q"] = torch.randn((b.nnz_q, 32, 128), generator=g, device=device).to(torch.bfloat16)
+    d["idx"] = i32(b.kv_indices, device)
+    attn = pka.BatchAttention(device=device)
+    d["info"] = attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, num_qo_heads=32,
+                          num_kv_heads=8, head_dim=128, page_size=page_size, layout=layout)
+    d["attn"] = attn
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty(b.nnz_q, 32, dtype=torch.float32, device=device)
+    dec = np.asarray(b.qo_lens) == 1
+    d["decode_bytes"] = int(np.sum(np.asarray(b.kv_lens)[dec])) * 8 * 128 * 2 * 2
+    pairs = 0
+    for q_, k_ in zip(np.asarray(b.qo_lens)[~dec], np.asarray(b.kv_lens)[~dec]):
+        pairs += int(q_) * (int(k_) - int(q_)) + int(q_) * (int(q_) + 1) // 2
+    d["prefill_flops"] = 4 * 128 * 32 * pairs
+    return d
+
+
+def mixed_step(d):
+    d["attn"].run(d["q"], d["k"], d["v"], d["idx"], out=d["o"], lse=d["lse"])
+
+
 def oracle_sample(seconds_budget=20.0, max_requests=None):
     """CPU oracle on the first requests of the batch-decode workload."""
     from oracle import ref
@@ -330,6 +365,11 @@ def profile_one(name, device, stream, steps, warmup, pk):
         ms = time_steps(lambda: (prefill_append(d), prefill_attn(d)), steps, warmup, stream)
         out = {"workload": "append_prefill", "ms": statistics.median(ms),
                "TFLOP/s": d["flops"] / (statistics.median(ms) * 1e-3) / 1e12}
+    elif name.startswith("mixed"):
+        P = 1 if name == "mixed1" else 16
+        d = mixed_setup(device, P, "NHD" if P == 1 else "HND")
+        ms = time_steps(lambda: mixed_step(d), steps, warmup, stream)
+        out = {"workload": f"mixed_step_page{P}", "ms": statistics.median(ms)}
     else:
         d = ragged_setup(device)
         ms = time_steps(lambda: ragged_step(d), steps, warmup, stream)
@@ -345,7 +385,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "ragged"],
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "ragged", "mixed1",
+                                                          "mixed16"],
                     help="all (default) prints the benchmark line; a single workload only runs "
                          "that workload's kernels (for profiling) and prints its numbers")
     args = ap.parse_args()
@@ -443,6 +484,26 @@ def main():
     del rg
     torch.cuda.empty_cache()
 
+    mixed = {}
+    for P, layout in ((1, "NHD"), (16, "HND")):
+        mx = mixed_setup(device, P, layout)
+        ms = statistics.median(time_steps(lambda: mixed_step(mx), 20, 3, stream))
+        t_roof = mx["decode_bytes"] / (pk["hbm_gbs"] * 1e9) + \
+            mx["prefill_flops"] / (pk["bf16_tflops"] * 1e12)
+        mixed[f"page{P}_{layout}"] = {
+            "ms_per_step": ms, "decode_kv_bytes": mx["decode_bytes"],
+            "prefill_flops": mx["prefill_flops"],
+            "decode_equiv_gbs": mx["decode_bytes"] / (ms * 1e-3) / 1e9,
+            "roofline_ms": t_roof * 1e3, "frac_of_summed_roofline": t_roof / (ms * 1e-3),
+            "plan": {k: v for k, v in mx["info"].as_dict().items()
+                     if k in ("num_decode_ctas", "num_prefill_ctas", "num_merge_tasks")}}
+        del mx
+        torch.cuda.empty_cache()
+    mixed["workload"] = ("mixed_step: 8 decodes kv U[32768,131072] + 120 decodes kv U[64,2048] + "
+                         "4 chunks of 512 (prefix U[0,8192]) (seed 1003), 32/8 heads, D 128; "
+                         "page 1 NHD and page 16 HND; one run() = decode + tensor-core + merge "
+                         "kernels; roofline = decode bytes / HBM peak + chunk FLOPs / bf16 peak")
+
     e2e = e2e_decode(d, min(args.steps, 500), 5, stream, device)
     if world > 1:
         import torch.distributed as dist
@@ -460,7 +521,8 @@ def main():
                        "kv_bytes_per_step": d["kv_bytes"], "bytes_per_step": d["bytes"],
                        "l2": "inputs (604 MB of K/V) larger than L2; no flush",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roof, "prefill": prefill, "ragged_custom_mask": ragged, "e2e": e2e,
+            "roofline": roof, "prefill": prefill, "ragged_custom_mask": ragged,
+            "mixed_step": mixed, "e2e": e2e,
             "gpu_launches": d["launches"] * args.steps,
             "clocks": clocks.summary(), "plan": d["info"].as_dict()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::prefetch_tmap(map);
     }
     uint32_t it = 0, q_uses = 0;
-    bool pending = false;  // tile it - 1 issued but not yet signalled
     for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
       const PkaWorkItem w = a.items[ii];
       const int n = num_tiles(w);
@@ -311,35 +310,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         load_kv_tile<D>(pp, map, pool, w, kb, smem_u32(ring + s * NB * BLK), smem_u32(&full[s]),
                         lane);
-        // Gathered rows are generic-proxy writes.  Each tile's copies form one
-        // commit group; once tile it is issued, wait for the group of tile
-        // it - 1, make its rows visible to the tensor cores and arrive for
-        // it, so the gathers of two tiles are in flight at a time.  (Safe:
-        // issuing tile it only needs stage it - ns released, which never
-        // depends on tile it - 1.)
-        // The last tile of an item is signalled at once: the next item's Q
-        // load waits for every QK^T of this item.
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        if (k == n - 1) {
-          asm volatile("cp.async.wait_group 0;" ::: "memory");
-          tc::fence_proxy_async_smem();
-          if (pending) mbar_arrive(smem_u32(&full[(it - 1) % ns]));
-          mbar_arrive(smem_u32(&full[s]));
-          pending = false;
-        } else {
-          if (pending) {
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-            tc::fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&full[(it - 1) % ns]));
-          }
-          pending = true;
-        }
+        // Gathered rows are generic-proxy writes: wait for this lane's copies,
+        // make them visible to the tensor cores, then arrive.
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        tc::fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&full[s]));
       }
-    }
-    if (pending) {  // only after an abort inside an item
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-      tc::fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&full[(it - 1) % ns]));
     }
     // Drain: the loads of the last stages must land before the CTA leaves.
     for (uint32_t k = it > (uint32_t)ns ? it - ns : 0; k < it; ++k)

@@ -20,8 +20,19 @@
 // (movmatrix).  A CTA writes the final bf16 output and base-2 LSE of a
 // request, or, when the plan split the request, a normalised fp32 partial
 // state for the merge kernel.
-#include "pka_device.cuh"
+//
+// HND pages of 8 or a multiple of 16 slots take a second staging layout: each
+// kv head's 16 keys arrive by TMA as [16 rows x 128 B] blocks with the
+// 128-byte swizzle (16-byte chunk c of row r stored at chunk c ^ (r & 7)),
+// and the ldmatrix addresses follow the swizzle; rows of a partial page are
+// gathered with 16-byte cp.async into the same layout.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "pka_internal.h"
+#include "tc_device.cuh"
 
 namespace pka {
 namespace {
@@ -40,6 +51,21 @@ struct Bars {
 
 // Bytes of one key row in a stage: the CTA's kv heads, plus 16 bytes of pad.
 __host__ __device__ constexpr int row_bytes(int hpc, int D) { return hpc * D * 2 + 16; }
+
+// Swizzled staging: one [16 keys x 64 dims] block is 2 KiB.
+constexpr int SWZ_BLK = TS * 128;
+
+struct DecodeMaps {
+  CUtensorMap k;  // HND pool {D, P, Hk, pages}, box {64, min(P, 16), 1, 1}
+  CUtensorMap v;
+};
+
+// Tiles start at multiples of 16 keys inside a request (the planner cuts
+// there) or at page boundaries, so with P = 8 or P a multiple of 16 every
+// box of min(P, 16) rows stays inside one page.
+__host__ __device__ inline bool use_swizzled(int layout, int P, int ragged) {
+  return layout == PKA_HND && !ragged && (P == 8 || P % 16 == 0);
+}
 
 __device__ __forceinline__ void record_timeout(int32_t* err, volatile int* abort_flag) {
   *abort_flag = 1;
@@ -121,9 +147,56 @@ __device__ __forceinline__ void issue_tile_copies(const AttnArgs& a, const PkaWo
   }
 }
 
+// Swizzled staging of keys [a0, a0 + n) (a0 is a multiple of 16): whole
+// boxes of R = min(P, 16) rows by TMA, the rest gathered with cp.async.
+// Rows of a tile of n keys that arrive by TMA (for expect_tx).
+__device__ __forceinline__ int swz_tma_rows(int P, int n) {
+  const int R = P < TS ? P : TS;
+  return (n / R) * R;
+}
+
 template <int D>
-__global__ void __launch_bounds__(288, 1) decode_kernel(const AttnArgs a, const int stages) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__device__ __forceinline__ void issue_tile_swizzled(const AttnArgs& a, const DecodeMaps& maps,
+                                                    const PkaWorkItem& w, int a0, int n, int hpc,
+                                                    uint32_t dK, uint32_t dV, uint32_t bar,
+                                                    int lane) {
+  constexpr int NB = D / 64;
+  const int P = a.page_size;
+  const int R = P < TS ? P : TS;
+  const int full_rows = (n / R) * R;
+  // TMA: box i covers tile rows [i R, (i + 1) R) of one kv head and one 64-dim block
+  const int nbox = full_rows / R;
+  for (int x = lane; x < nbox * hpc * NB * 2; x += 32) {
+    const int kv = x & 1, c = (x >> 1) % NB, h = ((x >> 1) / NB) % hpc, i = (x >> 1) / NB / hpc;
+    const int j = a0 + i * R;
+    const int page = a.kv_indices[w.kv_base + j / P];
+    const uint32_t dst = (kv ? dV : dK) + (h * NB + c) * SWZ_BLK + i * R * 128;
+    tc::tma_load_4d(dst, kv ? &maps.v : &maps.k, c * 64, j % P, w.kv_head0 + h, page, bar);
+  }
+  // cp.async: rows [full_rows, n), 16-byte chunks, swizzled by hand
+  constexpr int CH = D / 8;
+  const int rest = n - full_rows;
+  for (int x = lane; x < rest * hpc * CH * 2; x += 32) {
+    const int kv = x & 1, ch = (x >> 1) % CH, h = ((x >> 1) / CH) % hpc;
+    const int r = full_rows + (x >> 1) / CH / hpc;
+    const int j = a0 + r;
+    const int page = a.kv_indices[w.kv_base + j / P];
+    const int64_t off = (int64_t)page * a.page_stride +
+                        ((int64_t)(w.kv_head0 + h) * P + (j % P)) * D + ch * 8;
+    const uint32_t dst = (kv ? dV : dK) + (h * NB + ch / 8) * SWZ_BLK + r * 128 +
+                         (((ch % 8) ^ (r & 7)) * 16);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                 "l"((kv ? a.v : a.k) + off)
+                 : "memory");
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(288, 1)
+    decode_kernel(const __grid_constant__ DecodeMaps maps, const AttnArgs a, const int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
   __shared__ volatile int abort_flag;
   constexpr int KS = D / 16;  // k-steps of the QK^T product
   constexpr int MT = D / 16;  // 16-dim blocks of the P V product
@@ -131,8 +204,9 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const AttnArgs a, const 
   const int G = a.num_qo_heads / a.num_kv_heads;
   const int n_cons = hpc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool swz = use_swizzled(a.layout, a.page_size, a.kv_ragged);
   const int RS = row_bytes(hpc, D);
-  const int stage_bytes = TS * RS;
+  const int stage_bytes = swz ? hpc * (D / 64) * SWZ_BLK : TS * RS;
   uint8_t* sK = smem;
   uint8_t* sV = smem + stages * stage_bytes;
   const Bars bars{reinterpret_cast<uint64_t*>(smem + 2 * stages * stage_bytes), stages};
@@ -145,7 +219,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const AttnArgs a, const 
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(bars.full(s), 1);
+      mbar_init(bars.full(s), 33);  // expect_tx by lane 0 + the 32 producer lanes
       mbar_init(bars.empty(s), n_cons);
     }
     abort_flag = 0;
@@ -165,10 +239,20 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const AttnArgs a, const 
           break;
         }
         const int n = min(TS, w.t1 - a0);
-        if (lane == 0) mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * n * hpc * D * 2));
+        const int tx_rows = swz ? swz_tma_rows(a.page_size, n) : n;
+        if (lane == 0) mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * tx_rows * hpc * D * 2));
         __syncwarp();
-        issue_tile_copies<D>(a, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
-                             smem_u32(sV + s * stage_bytes), bars.full(s), lane);
+        if (swz) {
+          issue_tile_swizzled<D>(a, maps, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
+                                 smem_u32(sV + s * stage_bytes), bars.full(s), lane);
+          // gathered rows are generic-proxy writes: land, fence, then arrive
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        } else {
+          issue_tile_copies<D>(a, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
+                               smem_u32(sV + s * stage_bytes), bars.full(s), lane);
+        }
+        mbar_arrive(bars.full(s));
       }
     }
     // Drain: every issued tile's copies must land before the CTA leaves.
@@ -188,6 +272,12 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const AttnArgs a, const 
   const int mi = lane >> 3, mr = lane & 7;
   const uint32_t k_lane = (uint32_t)((mr + 8 * (mi & 1)) * RS + hl * D * 2 + 16 * (mi >> 1));
   const uint32_t v_lane = (uint32_t)((mr + 8 * (mi >> 1)) * RS + hl * D * 2 + 16 * (mi & 1));
+  // swizzled staging: chunk c (16 bytes) of key row r of kv head hl
+  const uint32_t hb = (uint32_t)(hl * (D / 64) * SWZ_BLK);
+  const int k_key = mr + 8 * (mi & 1), v_key = mr + 8 * (mi >> 1);
+  auto swz_addr = [&](int key, int c) -> uint32_t {
+    return hb + (uint32_t)((c >> 3) * SWZ_BLK + key * 128 + (((c & 7) ^ (key & 7)) << 4));
+  };
   const uint32_t sK0 = smem_u32(sK), sV0 = smem_u32(sV);
   const float sc = a.scale_log2;
   uint32_t it = 0;
@@ -227,7 +317,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const AttnArgs a, const 
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t af[4];
-        ldsm_x4(kb + k_lane + 32 * ks, af);
+        ldsm_x4(kb + (swz ? swz_addr(k_key, 2 * ks + (mi >> 1)) : k_lane + 32 * ks), af);
         mma16816(sacc, af, qf[ks][0], qf[ks][1]);
       }
       // keys grp and grp + 8 of the tile; heads 2qd, 2qd + 1
@@ -287,7 +377,7 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const AttnArgs a, const 
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         uint32_t af[4];
-        ldsm_x4_t(vb + v_lane + 32 * mt, af);
+        ldsm_x4_t(vb + (swz ? swz_addr(v_key, 2 * mt + (mi & 1)) : v_lane + 32 * mt), af);
         mma16816(acc[mt], af, pb0, pb1);
       }
       __syncwarp();
@@ -333,18 +423,54 @@ __global__ void __launch_bounds__(288, 1) decode_kernel(const AttnArgs a, const 
   }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// HND page pool {D, P, Hk, pages}: one box = min(P, 16) slots of one kv head
+// and 64 dims, 128-byte swizzle.
+bool encode_hnd(CUtensorMap* m, const void* base, const AttnArgs& a, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t P = a.page_size, Hk = a.num_kv_heads;
+  cuuint64_t dims[4] = {(cuuint64_t)D, P, Hk, (cuuint64_t)1 << 31};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, P * D * 2, (cuuint64_t)a.page_stride * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)(P < (uint64_t)TS ? P : TS), 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_t(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   const int hpc = a.heads_per_cta;
-  const int stage_bytes = 2 * TS * row_bytes(hpc, D);
+  const bool swz = use_swizzled(a.layout, a.page_size, a.kv_ragged);
+  DecodeMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if (swz && (!encode_hnd(&maps.k, a.k, a, D) || !encode_hnd(&maps.v, a.v, a, D)))
+    return cudaErrorInvalidValue;
+  const int stage_bytes = 2 * (swz ? hpc * (D / 64) * SWZ_BLK : TS * row_bytes(hpc, D));
   int stages = kStageBudget / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = (size_t)stages * stage_bytes + 2 * stages * sizeof(uint64_t);
+  // the swizzled blocks need 1024-byte alignment: pad the dynamic allocation
+  const size_t smem = 1024 + (size_t)stages * stage_bytes + 2 * stages * sizeof(uint64_t);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D><<<num_ctas, 32 * (hpc + 1), smem, stream>>>(a, stages);
+  decode_kernel<D><<<num_ctas, 32 * (hpc + 1), smem, stream>>>(maps, a, stages);
   return cudaGetLastError();
 }
 

@@ -216,7 +216,17 @@ void plan_decode(const pka_params* p, const Batch& b, int num_sms, PlanLists* L)
     std::vector<int> pieces;
     int64_t t = 0;
     do {
-      int64_t take = std::min<int64_t>(u.K - t, chunk - load);
+      // Cuts inside a request fall on 16-key tile boundaries, so that whole
+      // pages stay in one tile of the decode kernel.
+      int64_t take = u.K - t;
+      if (take > chunk - load) {
+        take = (chunk - load) / pka::kDecodeTileTokens * pka::kDecodeTileTokens;
+        if (take == 0) {  // no room for a whole tile: close this CTA
+          L->dec_cta_ptr.push_back((int)items.size());
+          load = 0;
+          continue;
+        }
+      }
       pieces.push_back((int)items.size());
       items.push_back(make_item(b, u.r, u.hg * hpc, hpc, 0, 1, (int)t, (int)(t + take)));
       t += take;

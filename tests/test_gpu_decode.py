@@ -29,7 +29,7 @@ def test_worked_lengths_as_decode(split):
 
 
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
-@pytest.mark.parametrize("page_size", [1, 3, 16, 32])
+@pytest.mark.parametrize("page_size", [1, 3, 8, 16, 32])
 @pytest.mark.parametrize("hq,hk,d", [(32, 8, 128), (8, 8, 64), (16, 8, 128), (16, 2, 64),
                                      (64, 8, 128), (32, 16, 128)])
 def test_decode_shapes(layout, page_size, hq, hk, d):

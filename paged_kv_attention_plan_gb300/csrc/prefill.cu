@@ -160,23 +160,22 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& pp, const CUte
         tc::tma_load_4d(d + c * BLK, map, c * 64, 0, w.kv_head0, page, bar);
     }
   }
-  // gathered rows: one lane per row (one page lookup), 16-byte chunks
-  // swizzled by hand (chunk ^ (row & 7))
+  // gathered rows: 16-byte chunks, swizzled by hand (chunk ^ (row & 7))
   constexpr int CH = D / 8;  // 16-byte chunks per row
   const int gathered = t.head_rows + (t.nrows - t.tail_start);
-  for (int q = lane; q < gathered; q += 32) {
+  for (int x = lane; x < gathered * CH; x += 32) {
+    const int q = x / CH, ch = x - q * CH;
     const int r = q < t.head_rows ? q : t.tail_start + (q - t.head_rows);
     const int j = kb + r;
-    const int pi = P == 1 ? j : j / P;
-    const int slot = j - pi * P;
+    const int pi = j / P;
     const int page = a.kv_indices[w.kv_base + pi];
-    const uint16_t* src = pool + (int64_t)page * a.page_stride +
-                          (nhd ? ((int64_t)slot * Hk + w.kv_head0) * D
-                               : ((int64_t)w.kv_head0 * P + slot) * D);
-    const uint32_t drow = dst + r * 128;
-#pragma unroll
-    for (int ch = 0; ch < CH; ++ch)
-      cp_async16(drow + (ch / 8) * BLK + (((ch % 8) ^ (r & 7)) * 16), src + ch * 8);
+    const int slot = j - pi * P;
+    const int64_t off = (int64_t)page * a.page_stride +
+                        (nhd ? ((int64_t)slot * Hk + w.kv_head0) * D
+                             : ((int64_t)w.kv_head0 * P + slot) * D) +
+                        ch * 8;
+    const uint32_t d = dst + (ch / 8) * BLK + r * 128 + (((ch % 8) ^ (r & 7)) * 16);
+    cp_async16(d, pool + off);
   }
 }
 

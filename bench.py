@@ -98,6 +98,21 @@ def flush_l2(buf):
     buf.add_(1)
 
 
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest value of x over all ranks (x itself when world == 1)."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: units of all ranks per second of the slowest rank."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 def time_steps(fn, steps, warmup, stream, l2_buf=None):
     """Per-step CUDA-event durations (ms) on the launching stream."""
     for _ in range(warmup):
@@ -432,14 +447,9 @@ def main():
             decode_step(d)
         ev1.record(stream)
         barrier()
-    total_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), world, device)
     ms = total_ms / args.steps
-    value = world * d["bytes"] / (ms * 1e-3) / 1e9
+    value = job_throughput(d["bytes"], ms, world) / 1e9
 
     # per-launch duration of the decode step (inputs > L2, so no flush is needed)
     per = time_steps(lambda: decode_step(d), 200, 5, stream)
@@ -506,10 +516,8 @@ def main():
 
     e2e = e2e_decode(d, min(args.steps, 500), 5, stream, device)
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e["ms_per_step"]], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["value"] = world * d["bytes"] / (float(t.item()) * 1e-3) / 1e9
+        e2e["value"] = job_throughput(d["bytes"], max_over_ranks(e2e["ms_per_step"], world, device),
+                                      world) / 1e9
     e2e.pop("ms_per_step")
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,

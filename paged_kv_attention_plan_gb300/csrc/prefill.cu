@@ -180,21 +180,34 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& pp, const CUte
 }
 
 // 128 consecutive mask bits starting at bit `start` (little-endian bit order);
-// bits at or past `limit` read as 0 and are never fetched.
+// bits at or past `limit` read as 0.  Five aligned 32-bit loads and funnel
+// shifts when the mask is 4-byte aligned and the words lie before the limit,
+// single bytes otherwise (near the end of the mask).
 __device__ __forceinline__ void load_mask_bits(const uint8_t* mask, int64_t start, int64_t limit,
                                                uint32_t (&bits)[4]) {
-  const int64_t byte0 = start >> 3;
-  const int sh = (int)(start & 7);
-  const int64_t last_byte = limit > start ? (limit - 1) >> 3 : byte0 - 1;
-  uint32_t by[17];
+  const int64_t last_byte = limit > start ? (limit - 1) >> 3 : (start >> 3) - 1;
+  const int64_t ab = (start >> 3) & ~int64_t(3);  // aligned byte of the first word
+  const int p = (int)(start - ab * 8);            // 0..31
+  if ((reinterpret_cast<uintptr_t>(mask) & 3) == 0 && ab + 20 <= last_byte + 1) {
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(mask + ab);
+    uint32_t wv[5];
 #pragma unroll
-  for (int b = 0; b < 17; ++b) by[b] = (byte0 + b <= last_byte) ? mask[byte0 + b] : 0u;
+    for (int i = 0; i < 5; ++i) wv[i] = __ldg(wp + i);
 #pragma unroll
-  for (int wd = 0; wd < 4; ++wd) {
-    const uint64_t v = (uint64_t)by[4 * wd] | ((uint64_t)by[4 * wd + 1] << 8) |
-                       ((uint64_t)by[4 * wd + 2] << 16) | ((uint64_t)by[4 * wd + 3] << 24) |
-                       ((uint64_t)by[4 * wd + 4] << 32);
-    bits[wd] = (uint32_t)(v >> sh);
+    for (int wd = 0; wd < 4; ++wd) bits[wd] = __funnelshift_r(wv[wd], wv[wd + 1], p);
+  } else {
+    const int64_t byte0 = start >> 3;
+    const int sh = (int)(start & 7);
+    uint32_t by[17];
+#pragma unroll
+    for (int b = 0; b < 17; ++b) by[b] = (byte0 + b <= last_byte) ? mask[byte0 + b] : 0u;
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+      const uint64_t v = (uint64_t)by[4 * wd] | ((uint64_t)by[4 * wd + 1] << 8) |
+                         ((uint64_t)by[4 * wd + 2] << 16) | ((uint64_t)by[4 * wd + 3] << 24) |
+                         ((uint64_t)by[4 * wd + 4] << 32);
+      bits[wd] = (uint32_t)(v >> sh);
+    }
   }
   // clear bits past the limit
   const int64_t keep = limit - start;

@@ -181,3 +181,17 @@ def test_mixed_step_full_size(page_size, layout):
     b.k_pool, b.v_pool = kh, vh
     o_ref, lse_ref = run_oracle(b, rows=rows)
     assert_parity(f64(o), f64(lse), o_ref, lse_ref, rows=rows)
+
+
+def test_custom_mask_unaligned_buffer():
+    """A packed mask that starts at an odd address (byte loads only)."""
+    b = W.make_ragged_batch(95, [200, 67], hq=8, hk=8, d=64, mask_mode="custom")
+    packed = ref.packbits_little(b.mask_bool)
+    store = torch.zeros(packed.size + 1, dtype=torch.uint8, device="cuda")
+    store[1:] = torch.from_numpy(packed).cuda()
+    attn = pka.BatchAttention()
+    attn.plan(b.qo_indptr, b.kv_indptr, None, num_qo_heads=8, num_kv_heads=8, head_dim=64,
+              mask_mode="custom", kv_ragged=True)
+    o, lse = attn.run(bf16(b.q), bf16(b.k_pool), bf16(b.v_pool), None, store[1:])
+    torch.cuda.synchronize()
+    assert_parity(f64(o), f64(lse), *run_oracle(b, packed_mask=packed))

@@ -318,7 +318,7 @@ def oracle_sample(seconds_budget=20.0, max_requests=None):
     b = W.batch_decode(seed=1001)
     done_bytes, t_used, r = 0, 0.0, 0
     limit = max_requests or b.batch_size
-    while t_used < seconds_budget and r < limit:
+    while (r == 0 or t_used < seconds_budget) and r < limit:
         t0 = time.perf_counter()
         ref.batch_attention(b.q, b.k_pool, b.v_pool, qo_indptr=b.qo_indptr,
                             kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,

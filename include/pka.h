@@ -89,7 +89,15 @@ typedef struct pka_params {
   int32_t split_mode;        /* pka_split_mode                                 */
   int32_t fixed_split_pages; /* pages per chunk for PKA_SPLIT_FIXED (>= 1)     */
   int32_t num_sms;           /* 0: query the current device; > 0: plan for it  */
-  int32_t reserved[5];       /* must be zero                                   */
+  /* CUDA-graph mode (graph_max_batch > 0): the plan image gets a fixed layout
+   * sized by these capacities and run() launches fixed grids, so a run()
+   * captured in a CUDA graph stays valid when later plans (same params,
+   * same workspaces) rewrite the image in place.  Split mode FIXED is not
+   * available in graph mode; prefill rows are not split. */
+  int32_t graph_max_batch;     /* the most requests of any plan                */
+  int32_t graph_max_qo_rows;   /* the most query rows; q and o hold this many   */
+  int32_t graph_max_kv_tokens; /* ragged K/V only: the most K/V rows            */
+  int32_t reserved[2];         /* must be zero                                  */
 } pka_params;
 
 /* Summary of a plan, filled by pka_plan (also when it fails with
@@ -130,6 +138,9 @@ pka_status pka_validate(const pka_params* params, int32_t batch, const int32_t* 
 /* Create / destroy the host plan object. */
 pka_status pka_plan_create(pka_plan_t* plan);
 void pka_plan_destroy(pka_plan_t plan);
+
+/* In graph mode pka_plan returns PKA_ERR_WORKSPACE when the batch exceeds the
+ * declared capacities (requests, query rows, ragged K/V rows). */
 
 /* plan(): inspect one batch on the host ("Deep Dive - FlashInfer", "Plan
  * then run"; "Load balancing and split-KV decisions").

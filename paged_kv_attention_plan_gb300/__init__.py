@@ -42,14 +42,19 @@ class BatchAttention:
 
     def plan(self, qo_indptr, kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, head_dim,
              page_size=1, layout="NHD", mask_mode="causal", sm_scale=0.0, kv_ragged=False,
-             split_mode="auto", fixed_split_pages=1, num_sms=0, stream=None):
+             split_mode="auto", fixed_split_pages=1, num_sms=0, graph_max_batch=0,
+             graph_max_qo_rows=0, graph_max_kv_tokens=0, stream=None):
         params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, layout, mask_mode,
-                             sm_scale, kv_ragged, split_mode, fixed_split_pages, num_sms)
+                             sm_scale, kv_ragged, split_mode, fixed_split_pages, num_sms,
+                             graph_max_batch, graph_max_qo_rows, graph_max_kv_tokens)
         s = pka_plan(self.handle, params, qo_indptr, kv_indptr, last_page_len, self.int_ws,
                      self.pinned, stream, check=False)
         if s == _WORKSPACE:
             info = pka_plan_get_info(self.handle)
             pka_plan_wait(self.handle)
+            if info.int_ws_bytes <= min(self.int_ws.numel(), self.pinned.numel()):
+                # not a buffer size: the batch exceeds the graph-mode capacities
+                raise PkaError(s, "pka_plan: " + pka_last_error())
             n = max(int(info.int_ws_bytes), self.int_ws.numel())
             self.int_ws = torch.empty(n, dtype=torch.uint8, device=self.device)
             self.pinned = torch.empty(n, dtype=torch.uint8, pin_memory=True)

@@ -36,7 +36,9 @@ class pka_params(ctypes.Structure):
                 ("layout", ctypes.c_int32), ("mask_mode", ctypes.c_int32),
                 ("sm_scale", ctypes.c_float), ("kv_ragged", ctypes.c_int32),
                 ("split_mode", ctypes.c_int32), ("fixed_split_pages", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("num_sms", ctypes.c_int32), ("graph_max_batch", ctypes.c_int32),
+                ("graph_max_qo_rows", ctypes.c_int32), ("graph_max_kv_tokens", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class pka_plan_info(ctypes.Structure):
@@ -174,7 +176,8 @@ def _stream(stream) -> int | None:
 
 def make_params(num_qo_heads, num_kv_heads, head_dim, page_size=1, layout="NHD",
                 mask_mode="causal", sm_scale=0.0, kv_ragged=False, split_mode="auto",
-                fixed_split_pages=1, num_sms=0) -> pka_params:
+                fixed_split_pages=1, num_sms=0, graph_max_batch=0, graph_max_qo_rows=0,
+                graph_max_kv_tokens=0) -> pka_params:
     p = pka_params()
     p.num_qo_heads, p.num_kv_heads, p.head_dim = num_qo_heads, num_kv_heads, head_dim
     p.page_size = page_size
@@ -187,6 +190,9 @@ def make_params(num_qo_heads, num_kv_heads, head_dim, page_size=1, layout="NHD",
                     [split_mode] if isinstance(split_mode, str) else split_mode)
     p.fixed_split_pages = fixed_split_pages
     p.num_sms = num_sms
+    p.graph_max_batch = graph_max_batch
+    p.graph_max_qo_rows = graph_max_qo_rows
+    p.graph_max_kv_tokens = graph_max_kv_tokens
     return p
 
 

@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(288, 1)
   const Bars bars{reinterpret_cast<uint64_t*>(smem + 2 * stages * stage_bytes), stages};
 
   const int i0 = a.cta_ptr[blockIdx.x], i1 = a.cta_ptr[blockIdx.x + 1];
+  if (i0 >= i1) return;  // an empty CTA of a fixed (graph mode) grid
   // Rows of a partial tile that no copy writes must hold finite values (their
   // P is 0, and 0 * NaN would poison O): zero the stages once.
   for (int x = threadIdx.x; x < 2 * stages * stage_bytes / 16; x += blockDim.x)

@@ -24,7 +24,8 @@ struct PkaImageHeader {
   int32_t off_prefill_items;     // PkaWorkItem[num_prefill_items]
   int32_t off_merge_tasks;       // PkaMergeTask[num_merge_tasks]
   int32_t decode_heads_per_cta;  // kv heads one decode CTA covers
-  int32_t reserved[2];
+  int32_t graph_mode;            // 1: fixed layout sized by the graph capacities
+  int32_t reserved;
 };
 
 // One unit of attention work: a block of kv heads (decode) or one kv head

@@ -9,6 +9,7 @@
 // policy here is ours (see split_decode / split_prefill below).
 #include <algorithm>
 #include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <functional>
@@ -28,6 +29,8 @@ struct pka_plan_s {
   cudaEvent_t event = nullptr;
   bool copy_pending = false;
   int device = -1;
+  int32_t layout_records = 0;  // partial records the float workspace is laid out for
+  int32_t merge_capacity = 0;  // graph mode: merge tasks the image has room for
 };
 
 namespace {
@@ -44,8 +47,13 @@ pka_status cuda_fail(cudaError_t e, const char* where) {
 
 bool params_ok(const pka_params* p) {
   if (!p) return false;
-  for (int i = 0; i < 5; ++i)
+  for (int i = 0; i < 2; ++i)
     if (p->reserved[i] != 0) return false;
+  if (p->graph_max_batch < 0 || p->graph_max_qo_rows < 0 || p->graph_max_kv_tokens < 0)
+    return false;
+  if (p->graph_max_batch == 0 && (p->graph_max_qo_rows || p->graph_max_kv_tokens)) return false;
+  if (p->graph_max_batch > 0 && p->graph_max_qo_rows < 1) return false;
+  if (p->graph_max_batch > 0 && p->kv_ragged && p->graph_max_kv_tokens < 1) return false;
   if (p->num_qo_heads < 1 || p->num_kv_heads < 1) return false;
   if (p->layout != PKA_NHD && p->layout != PKA_HND) return false;
   if (p->mask_mode < PKA_MASK_NONE || p->mask_mode > PKA_MASK_CUSTOM) return false;
@@ -61,7 +69,35 @@ pka_status check_supported(const pka_params* p) {
   int g = p->num_qo_heads / p->num_kv_heads;
   if (g != 1 && g != 2 && g != 4 && g != 8) return PKA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128) return PKA_ERR_UNSUPPORTED;
+  if (p->graph_max_batch > 0 && p->split_mode == PKA_SPLIT_FIXED) return PKA_ERR_UNSUPPORTED;
   return PKA_OK;
+}
+
+bool graph_mode(const pka_params* p) { return p->graph_max_batch > 0; }
+
+// Graph mode: section capacities of the plan image, from the declared limits.
+// Decode: units (request, head block) <= B * Hk / hpc; the AUTO split closes a
+// CTA only once it holds more than chunk - 16 >= 3/4 chunk keys, so it makes
+// at most 4/3 * num_sms + 2 CTAs and every item either ends a unit or closes
+// a CTA.  Tensor-core rows are not split in graph mode: one item per
+// (request, kv head, query tile) and sum_r ceil(Q_r / tq) <= ceil(R / tq) + B.
+struct GraphCaps {
+  int64_t dec_items = 0, pre_items = 0, merges = 0, records = 0;
+};
+
+GraphCaps graph_caps(const pka_params* p, int num_sms) {
+  GraphCaps c;
+  const int64_t B = p->graph_max_batch, R = p->graph_max_qo_rows;
+  const int g = p->num_qo_heads / p->num_kv_heads;
+  const int hpc = pka::decode_heads_per_cta(p->num_kv_heads, g);
+  const int tq = 2 * (pka::kPrefillTileRows / g);
+  c.dec_items = B * (p->num_kv_heads / hpc) + 2 * (int64_t)num_sms + 2;
+  c.pre_items = (int64_t)p->num_kv_heads * ((R + tq - 1) / tq + B);
+  if (p->split_mode == PKA_SPLIT_AUTO) {
+    c.merges = B * p->num_qo_heads;
+    c.records = c.dec_items * hpc * g;
+  }
+  return c;
 }
 
 struct Batch {
@@ -268,7 +304,8 @@ void plan_prefill(const pka_params* p, const Batch& b, int num_sms, PlanLists* L
   int64_t chunk = 0;  // keys per piece, 0 = whole range
   if (p->split_mode == PKA_SPLIT_FIXED) {
     chunk = (int64_t)p->fixed_split_pages * (p->kv_ragged ? 1 : p->page_size);
-  } else if (p->split_mode == PKA_SPLIT_AUTO && (int64_t)units.size() < 2 * num_sms) {
+  } else if (p->split_mode == PKA_SPLIT_AUTO && !graph_mode(p) &&
+             (int64_t)units.size() < 2 * num_sms) {
     int64_t per_cta = std::max<int64_t>(4, (total_tiles + num_sms - 1) / num_sms);
     chunk = per_cta * pka::kPrefillTileKeys;
   }
@@ -309,6 +346,42 @@ void plan_prefill(const pka_params* p, const Batch& b, int num_sms, PlanLists* L
     L->pre_cta_ptr.push_back((int)sorted.size());
   }
   items.swap(sorted);
+}
+
+// Graph mode: deal the planner's CTAs onto exactly `ctas` CTAs, heaviest
+// first onto the least loaded one, so that the grid never changes.
+void fold_ctas(std::vector<int32_t>& cta_ptr, std::vector<PkaWorkItem>& items, int ctas) {
+  const int n = (int)cta_ptr.size() - 1;
+  if (n <= ctas) {
+    cta_ptr.resize(ctas + 1, cta_ptr.back());
+    return;
+  }
+  std::vector<int64_t> cost(n, 0);
+  for (int c = 0; c < n; ++c)
+    for (int i = cta_ptr[c]; i < cta_ptr[c + 1]; ++i) cost[c] += (items[i].t1 - items[i].t0) + 64;
+  std::vector<int> order(n);
+  for (int c = 0; c < n; ++c) order[c] = c;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+  using Slot = std::pair<int64_t, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push({0, c});
+  std::vector<std::vector<int>> per(ctas);
+  for (int c : order) {
+    Slot s = heap.top();
+    heap.pop();
+    per[s.second].push_back(c);
+    heap.push({s.first + cost[c], s.second});
+  }
+  std::vector<PkaWorkItem> sorted;
+  sorted.reserve(items.size());
+  std::vector<int32_t> ptr{0};
+  for (int c = 0; c < ctas; ++c) {
+    for (int v : per[c])
+      for (int i = cta_ptr[v]; i < cta_ptr[v + 1]; ++i) sorted.push_back(items[i]);
+    ptr.push_back((int32_t)sorted.size());
+  }
+  items.swap(sorted);
+  cta_ptr.swap(ptr);
 }
 
 size_t align_words(size_t w) { return (w + 15) & ~size_t(15); }
@@ -371,6 +444,7 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
                     void* pinned_h, size_t pinned_bytes, void* stream) {
   if (!plan || !params_ok(p)) return PKA_ERR_INVALID_ARG;
   plan->planned = false;
+  plan->info = pka_plan_info{};
   pka_status s = check_supported(p);
   if (s != PKA_OK) return s;
   Batch b;
@@ -389,9 +463,34 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
     }
   }
 
+  const bool graph = graph_mode(p);
+  if (graph && (batch > p->graph_max_batch || b.nnz_q > p->graph_max_qo_rows ||
+                (p->kv_ragged && b.total_kv > p->graph_max_kv_tokens))) {
+    pka::set_last_error("batch exceeds the graph-mode capacities");
+    return PKA_ERR_WORKSPACE;
+  }
+
   PlanLists L;
   plan_decode(p, b, num_sms, &L);
   plan_prefill(p, b, num_sms, &L);
+  GraphCaps caps;
+  if (graph) {
+    caps = graph_caps(p, num_sms);
+    fold_ctas(L.dec_cta_ptr, L.dec_items, num_sms);
+    fold_ctas(L.pre_cta_ptr, L.pre_items, num_sms);
+    if ((int64_t)L.dec_items.size() > caps.dec_items ||
+        (int64_t)L.pre_items.size() > caps.pre_items || (int64_t)L.merges.size() > caps.merges ||
+        L.records > caps.records) {
+      pka::set_last_error("plan outgrew the graph-mode image capacities");
+      return PKA_ERR_WORKSPACE;
+    }
+  }
+  // Section sizes: what this plan holds, or the fixed capacities in graph mode.
+  const int64_t n_dec_ptr = (int64_t)L.dec_cta_ptr.size(), n_pre_ptr = (int64_t)L.pre_cta_ptr.size();
+  const int64_t n_dec = graph ? caps.dec_items : (int64_t)L.dec_items.size();
+  const int64_t n_pre = graph ? caps.pre_items : (int64_t)L.pre_items.size();
+  const int64_t n_merge = graph ? caps.merges : (int64_t)L.merges.size();
+  const int64_t layout_records = graph ? caps.records : L.records;
 
   PkaImageHeader h{};
   h.magic = PKA_IMAGE_MAGIC;
@@ -403,24 +502,31 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   h.num_partial_records = L.records;
   h.decode_heads_per_cta =
       pka::decode_heads_per_cta(p->num_kv_heads, p->num_qo_heads / p->num_kv_heads);
+  h.graph_mode = graph ? 1 : 0;
+  constexpr size_t kItemWords = sizeof(PkaWorkItem) / 4, kMergeWords = sizeof(PkaMergeTask) / 4;
   size_t w = align_words(sizeof(PkaImageHeader) / 4);
   h.off_decode_cta_ptr = (int)w;
-  w = align_words(w + L.dec_cta_ptr.size());
+  w = align_words(w + n_dec_ptr);
   h.off_decode_items = (int)w;
-  w = align_words(w + L.dec_items.size() * (sizeof(PkaWorkItem) / 4));
+  w = align_words(w + n_dec * kItemWords);
   h.off_prefill_cta_ptr = (int)w;
-  w = align_words(w + L.pre_cta_ptr.size());
+  w = align_words(w + n_pre_ptr);
   h.off_prefill_items = (int)w;
-  w = align_words(w + L.pre_items.size() * (sizeof(PkaWorkItem) / 4));
+  w = align_words(w + n_pre * kItemWords);
   h.off_merge_tasks = (int)w;
-  w = align_words(w + L.merges.size() * (sizeof(PkaMergeTask) / 4));
+  w = align_words(w + n_merge * kMergeWords);
+  if (w > (size_t)INT32_MAX || layout_records > INT32_MAX / 256) {
+    pka::set_last_error("plan image or partial records exceed 2^31");
+    return PKA_ERR_UNSUPPORTED;
+  }
   h.total_words = (int)w;
 
   pka_plan_info info{};
   info.int_ws_bytes = (uint64_t)w * 4;
-  size_t rec_o = (size_t)L.records * p->head_dim * 4;
+  size_t rec_o = (size_t)layout_records * p->head_dim * 4;
   size_t rec_o_al = (rec_o + 255) & ~size_t(255);
-  info.float_ws_bytes = L.records ? rec_o_al + (((size_t)L.records * 4 + 255) & ~size_t(255)) : 0;
+  info.float_ws_bytes =
+      layout_records ? rec_o_al + (((size_t)layout_records * 4 + 255) & ~size_t(255)) : 0;
   info.num_requests = batch;
   info.nnz_qo = b.nnz_q;
   info.total_kv = b.total_kv;
@@ -440,8 +546,20 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
     if (cudaEventSynchronize(plan->event) != cudaSuccess) return PKA_ERR_CUDA;
     plan->copy_pending = false;
   }
+  // Word ranges of the image that carry this plan: all of it, or in graph mode
+  // the used head of each fixed-size section (the kernels read no further).
+  std::vector<std::pair<size_t, size_t>> ranges;
+  if (graph) {
+    ranges.push_back({0, h.off_decode_items + L.dec_items.size() * kItemWords});
+    ranges.push_back({(size_t)h.off_prefill_cta_ptr,
+                      h.off_prefill_items + L.pre_items.size() * kItemWords - h.off_prefill_cta_ptr});
+    if (!L.merges.empty())
+      ranges.push_back({(size_t)h.off_merge_tasks, L.merges.size() * kMergeWords});
+  } else {
+    ranges.push_back({0, w});
+  }
   int32_t* img = static_cast<int32_t*>(pinned_h);
-  std::memset(img, 0, info.int_ws_bytes);
+  for (const auto& r : ranges) std::memset(img + r.first, 0, r.second * 4);
   std::memcpy(img, &h, sizeof(h));
   std::memcpy(img + h.off_decode_cta_ptr, L.dec_cta_ptr.data(), L.dec_cta_ptr.size() * 4);
   if (!L.dec_items.empty())
@@ -455,12 +573,16 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   plan->params = *p;
   plan->hdr = h;
   plan->int_ws_d = static_cast<int32_t*>(int_ws_d);
+  plan->layout_records = (int32_t)layout_records;
+  plan->merge_capacity = (int32_t)n_merge;
   if (int_ws_d) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (!plan->event) e = cudaEventCreateWithFlags(&plan->event, cudaEventDisableTiming);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(int_ws_d, img, info.int_ws_bytes, cudaMemcpyHostToDevice, st);
+    for (const auto& r : ranges)
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(static_cast<int32_t*>(int_ws_d) + r.first, img + r.first, r.second * 4,
+                            cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaEventRecord(plan->event, st);
     if (e != cudaSuccess) return cuda_fail(e, "plan copy");
     plan->copy_pending = true;
@@ -504,7 +626,8 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int g = p->num_qo_heads / p->num_kv_heads;
   float scale = p->sm_scale > 0.f ? p->sm_scale : 1.0f / std::sqrt((float)p->head_dim);
-  size_t rec_o = (size_t)h.num_partial_records * p->head_dim * 4;
+  const bool graph = graph_mode(p);
+  size_t rec_o = (size_t)plan->layout_records * p->head_dim * 4;
   size_t rec_o_al = (rec_o + 255) & ~size_t(255);
 
   AttnArgs a{};
@@ -527,23 +650,28 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
   a.heads_per_cta = h.decode_heads_per_cta;
   a.scale_log2 = scale * 1.4426950408889634f;
 
-  if (h.num_decode_items > 0) {
+  // Graph mode launches every kernel on its fixed grid, whatever this plan
+  // holds, so that a captured run() serves every later plan.
+  if (graph || h.num_decode_items > 0) {
     a.cta_ptr = plan->int_ws_d + h.off_decode_cta_ptr;
     a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_decode_items);
     cudaError_t e = pka::launch_decode(a, h.num_decode_ctas, p->head_dim, g, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
-  if (h.num_prefill_items > 0) {
+  if (graph || h.num_prefill_items > 0) {
     a.cta_ptr = plan->int_ws_d + h.off_prefill_cta_ptr;
     a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_prefill_items);
-    cudaError_t e = pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g,
-                                        plan->info.nnz_qo, plan->info.total_kv, st);
+    // the Q (and ragged K/V) tensor maps span the buffers' declared rows
+    const int rows = graph ? p->graph_max_qo_rows : plan->info.nnz_qo;
+    const int64_t kv_rows = graph ? p->graph_max_kv_tokens : plan->info.total_kv;
+    cudaError_t e = pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g, rows, kv_rows, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
-  if (h.num_merge_tasks > 0) {
+  if (graph ? plan->merge_capacity > 0 : h.num_merge_tasks > 0) {
     pka::MergeArgs m{};
     m.tasks = reinterpret_cast<const PkaMergeTask*>(plan->int_ws_d + h.off_merge_tasks);
-    m.num_tasks = h.num_merge_tasks;
+    m.num_tasks = graph ? plan->merge_capacity : h.num_merge_tasks;
+    if (graph) m.num_tasks_dev = plan->int_ws_d + offsetof(PkaImageHeader, num_merge_tasks) / 4;
     m.heads = p->num_qo_heads;
     m.part_o = a.part_o;
     m.part_lse = a.part_lse;

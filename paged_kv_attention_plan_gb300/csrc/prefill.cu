@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i0 = a.cta_ptr[blockIdx.x], i1 = a.cta_ptr[blockIdx.x + 1];
+  if (i0 >= i1) return;  // an empty CTA of a fixed (graph mode) grid: no TMEM, no barriers
   const int G = pp.group;
   const int TQ = BM / G;  // query tokens of one 128-row tile
 

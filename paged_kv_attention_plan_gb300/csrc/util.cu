@@ -52,13 +52,10 @@ namespace {
 // result is a zero vector and -inf.  One warp per (row, head).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
+__device__ __forceinline__ void merge_one(const MergeArgs& a, const int task, const int lane) {
   constexpr int PER = D / 32;  // dims per lane
-  const int task = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   int out_row, head, rec_first, nslots, stride;
   if (a.tasks) {
-    if (task >= a.num_tasks) return;
     const PkaMergeTask t = a.tasks[task];
     out_row = t.out_row;
     head = t.head;
@@ -66,7 +63,6 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
     nslots = t.nslots;
     stride = t.rec_stride;
   } else {
-    if (task >= a.rows * a.heads) return;
     out_row = task / a.heads;
     head = task % a.heads;
     const int s0 = a.indptr[out_row], s1 = a.indptr[out_row + 1];
@@ -113,6 +109,17 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   }
   if (lane == 0 && a.lse)
     a.lse[(int64_t)out_row * a.heads + head] = shift == -INFINITY ? -INFINITY : shift + log2f(z);
+}
+
+// Warps stride over the tasks.  With num_tasks_dev set (graph mode) the count
+// is read from the device plan image, bounded by the list's capacity.
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
+  int n = a.tasks ? a.num_tasks : a.rows * a.heads;
+  if (a.tasks && a.num_tasks_dev) n = min(max(*a.num_tasks_dev, 0), a.num_tasks);
+  const int lane = threadIdx.x & 31;
+  for (int task = blockIdx.x * 8 + (threadIdx.x >> 5); task < n; task += gridDim.x * 8)
+    merge_one<D>(a, task, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -194,7 +201,7 @@ int grid_for(int64_t work, int block) {
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   const int tasks = a.tasks ? a.num_tasks : a.rows * a.heads;
   if (tasks <= 0) return cudaSuccess;
-  const int blocks = (tasks + 7) / 8;
+  const int blocks = grid_for(tasks, 8);
   if (a.head_dim == 128)
     merge_kernel<128><<<blocks, 256, 0, stream>>>(a);
   else

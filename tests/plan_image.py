@@ -4,7 +4,7 @@ import numpy as np
 HEADER = ["magic", "total_words", "num_decode_ctas", "num_decode_items", "num_prefill_ctas",
           "num_prefill_items", "num_merge_tasks", "num_partial_records", "off_decode_cta_ptr",
           "off_decode_items", "off_prefill_cta_ptr", "off_prefill_items", "off_merge_tasks",
-          "decode_heads_per_cta"]
+          "decode_heads_per_cta", "graph_mode"]
 ITEM = ["req", "kv_head0", "n_kv_heads", "q_row0", "q_local0", "q_count", "qo_len", "kv_len",
         "kv_base", "t0", "t1", "out_rec", "mask_lo", "mask_hi", "flags", "reserved"]
 MERGE = ["out_row", "head", "rec_first", "nslots", "rec_stride"]

@@ -51,3 +51,119 @@ def test_captured_run_replays_with_new_contents():
         torch.cuda.synchronize()
         assert pka.pka_get_device_error() == 0
         assert_parity(f64(o), f64(lse), *run_oracle(b))
+
+
+# ---------------------------------------------------------------------------
+# Graph mode: one capture serves later plans of other batches
+# ---------------------------------------------------------------------------
+PAGED_SPECS = [
+    ([1, 40, 1, 300, 1], [900, 40, 2000, 700, 17]),          # mixed
+    ([1] * 8, [5000, 1, 33, 800, 64, 2, 4096, 100]),          # decode only, at the batch cap
+    ([600], [3000]),                                          # one long prefill
+    ([2, 1], [2, 9000]),                                      # tiny prefill, long decode
+    ([100, 200, 1, 1, 300, 1, 7, 1], [100, 1200, 1, 5, 310, 9000, 7, 64]),
+]
+
+
+@pytest.mark.parametrize("layout,page_size", [("HND", 16), ("NHD", 1)])
+def test_graph_mode_capture_serves_new_plans(layout, page_size):
+    hq, hk, d = 32, 8, 128
+    max_batch, max_rows = 8, 640
+    pool_pages = (20000 + page_size - 1) // page_size + 8 * 2
+    batches = [W.make_paged_batch(50 + i, qo, kv, page_size=page_size, layout=layout, hq=hq,
+                                  hk=hk, d=d, pool_pages=pool_pages)
+               for i, (qo, kv) in enumerate(PAGED_SPECS)]
+    shape = batches[0].k_pool.shape
+    q_buf = torch.zeros(max_rows, hq, d, dtype=torch.bfloat16, device="cuda")
+    o_buf = torch.zeros_like(q_buf)
+    lse_buf = torch.zeros(max_rows, hq, dtype=torch.float32, device="cuda")
+    k_buf = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+    v_buf = torch.zeros_like(k_buf)
+    idx_buf = torch.zeros(pool_pages, dtype=torch.int32, device="cuda")
+    attn = pka.BatchAttention()
+    stream = torch.cuda.Stream()
+    kw = dict(num_qo_heads=hq, num_kv_heads=hk, head_dim=d, page_size=page_size, layout=layout,
+              graph_max_batch=max_batch, graph_max_qo_rows=max_rows, stream=stream)
+
+    def load(b):
+        q_buf[:b.nnz_q].copy_(bf16(b.q))
+        k_buf.copy_(bf16(b.k_pool))
+        v_buf.copy_(bf16(b.v_pool))
+        idx_buf[:len(b.kv_indices)].copy_(i32(b.kv_indices))
+        torch.cuda.synchronize()
+        attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, **kw)
+
+    def call():
+        attn.run(q_buf, k_buf, v_buf, idx_buf, out=o_buf, lse=lse_buf, stream=stream)
+
+    load(batches[0])
+    with torch.cuda.stream(stream):
+        call()  # first call outside capture (one-time set-up)
+    torch.cuda.synchronize()
+    ws = (attn.int_ws.data_ptr(), attn.float_ws.data_ptr())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+    torch.cuda.synchronize()
+    for b in batches[1:] + batches[:1]:
+        load(b)
+        assert (attn.int_ws.data_ptr(), attn.float_ws.data_ptr()) == ws
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert pka.pka_get_device_error() == 0
+        n = b.nnz_q
+        assert_parity(f64(o_buf[:n]), f64(lse_buf[:n]), *run_oracle(b))
+
+
+def test_graph_mode_ragged_custom_mask():
+    from oracle import ref
+    hq, hk, d = 16, 4, 64
+    max_batch, max_rows = 6, 700
+    specs = [[300, 1, 200, 100], [1, 1, 1], [700], [64, 65, 1, 190, 2, 3]]
+    batches = [W.make_ragged_batch(60 + i, lens, hq=hq, hk=hk, d=d) for i, lens in
+               enumerate(specs)]
+    max_bits = max(int(np.sum(np.asarray(s) ** 2)) for s in specs)
+    q_buf = torch.zeros(max_rows, hq, d, dtype=torch.bfloat16, device="cuda")
+    o_buf, lse_buf = torch.zeros_like(q_buf), torch.zeros(max_rows, hq, device="cuda")
+    k_buf = torch.zeros(max_rows, hk, d, dtype=torch.bfloat16, device="cuda")
+    v_buf = torch.zeros_like(k_buf)
+    m_buf = torch.zeros((max_bits + 7) // 8 + 16, dtype=torch.uint8, device="cuda")
+    attn = pka.BatchAttention()
+    stream = torch.cuda.Stream()
+    kw = dict(num_qo_heads=hq, num_kv_heads=hk, head_dim=d, mask_mode="custom", kv_ragged=True,
+              graph_max_batch=max_batch, graph_max_qo_rows=max_rows,
+              graph_max_kv_tokens=max_rows, stream=stream)
+
+    def load(b):
+        n = b.nnz_q
+        packed = ref.packbits_little(b.mask_bool.astype(bool))
+        q_buf[:n].copy_(bf16(b.q))
+        k_buf[:n].copy_(bf16(b.k_pool))
+        v_buf[:n].copy_(bf16(b.v_pool))
+        m_buf[:len(packed)].copy_(torch.from_numpy(packed))
+        torch.cuda.synchronize()
+        attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, **kw)
+        return packed
+
+    def call():
+        attn.run(q_buf, k_buf, v_buf, None, m_buf, out=o_buf, lse=lse_buf, stream=stream)
+
+    load(batches[0])
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+    torch.cuda.synchronize()
+    for b in batches[1:] + batches[:1]:
+        packed = load(b)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert pka.pka_get_device_error() == 0
+        n = b.nnz_q
+        assert_parity(f64(o_buf[:n]), f64(lse_buf[:n]), *run_oracle(b, packed_mask=packed))

@@ -22,11 +22,16 @@ pages it cites; nothing is blocked, fused or reordered:
 * "GPU attention backends: FlashInfer and FlashAttention" (mini-sglang):
   sections "FlashInfer: plan and run" (page-size-1 view of a token pool) and
   "FlashAttention: a page-number table" (page-number table to CSR).
+* "KV-Cache layouts", section "Multi-level cascade inference data layout"
+  (per-level qo_indptr / kv_indptr / kv_indices / last_page_len over one
+  pool): cascade_attention.
 
 Readings where the pages are silent (each is listed in the design notes):
 bit 1 of a custom mask keeps a key; the mask is applied after scaling; a row
 that sees no key returns a zero vector and lse = -inf; new tokens of a request
-occupy its last qo_len logical positions; qo head h reads kv head h // g.
+occupy its last qo_len logical positions; qo head h reads kv head h // g; in
+a cascade, keys of levels above the last are all visible to the rows below
+them and only the last level carries the mask.
 
 Pins (tests that tie this module to something other than itself) live in
 tests/test_oracle_*.py; every function below has at least one.
@@ -290,6 +295,88 @@ def batch_attention(q_bits, k_pool_bits, v_pool_bits, *, qo_indptr, kv_indptr, k
                     o[row, h], lse[row, h] = direct_state(s, vr[keys, kh, :])
                 else:
                     o[row, h], lse[row, h] = np.zeros(head_dim), -math.inf
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Multi-level cascade ("KV-Cache layouts", "Multi-level cascade inference data
+# layout"; "Deep Dive - FlashInfer", "Core mechanism": the attention state is
+# the unit that composes across shared prefixes)
+# ---------------------------------------------------------------------------
+
+def _node_of(qo_indptr, row: int) -> int:
+    """Index n of the node whose query range [qo_indptr[n], qo_indptr[n+1]) holds ``row``."""
+    for n in range(len(qo_indptr) - 1):
+        if int(qo_indptr[n]) <= row < int(qo_indptr[n + 1]):
+            return n
+    raise ValueError(f"row {row} is in no node")
+
+
+def _node_kv_len(level, n: int, page_size: int) -> int:
+    pages = int(level["kv_indptr"][n + 1]) - int(level["kv_indptr"][n])
+    if pages == 0:
+        return 0  # a node without keys (shared levels only)
+    return kv_len_from_pages(range(pages), int(level["last_page_len"][n]), page_size)
+
+
+def cascade_attention(q_bits, k_pool_bits, v_pool_bits, *, levels, page_size, num_qo_heads,
+                      num_kv_heads, layout="NHD", mask_mode="causal", sm_scale=None):
+    """Reference output of a multi-level cascade over one page pool.
+
+    ``levels`` lists, from the root, dicts with the level's own qo_indptr,
+    kv_indptr, kv_indices and last_page_len (the page-table semantics of every
+    other call).  Every level splits the same query rows into nodes.  A row
+    sees, at each level but the last, every key of the node holding it (a
+    shared prefix lies wholly before the row's own tokens); at the last level
+    the keys of its node that ``mask_mode`` leaves visible, with that node's
+    (Q, K) and the row's index inside it.  The state is the softmax over the
+    union of those key sets, taken in one pass: no merge.  A shared-level node
+    may hold no pages."""
+    q = bf16_bits_to_f64(q_bits)
+    nnz, _, head_dim = q.shape
+    group = num_qo_heads // num_kv_heads
+    scale = (1.0 / math.sqrt(head_dim)) if not sm_scale else float(sm_scale)
+    last = len(levels) - 1
+    for lv in levels:
+        if int(lv["qo_indptr"][-1]) != nnz:
+            raise ValueError("every level must cover all query rows")
+    cache = {}
+
+    def node_kv(li, n):
+        if (li, n) not in cache:
+            lv = levels[li]
+            klen = _node_kv_len(lv, n, page_size)
+            kv = [bf16_bits_to_f64(gather_request_kv(
+                pool, layout=layout, page_size=page_size, kv_indptr=lv["kv_indptr"],
+                kv_indices=lv["kv_indices"], req=n, kv_len=klen)) for pool in (k_pool_bits,
+                                                                               v_pool_bits)]
+            cache[(li, n)] = (klen, kv[0], kv[1])
+        return cache[(li, n)]
+
+    o = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:2])
+    for row in range(nnz):
+        ks, vs = [], []
+        for li, lv in enumerate(levels):
+            n = _node_of(lv["qo_indptr"], row)
+            klen, kr, vr = node_kv(li, n)
+            if li < last:
+                keys = list(range(klen))
+            else:
+                qlen = int(lv["qo_indptr"][n + 1]) - int(lv["qo_indptr"][n])
+                if mask_mode == "causal" and klen < qlen:
+                    raise ValueError("causal attention needs kv_len >= qo_len at the last level")
+                keys = visible_keys(mask_mode, row - int(lv["qo_indptr"][n]), qlen, klen)
+            ks.append(kr[keys])
+            vs.append(vr[keys])
+        kc, vc = np.concatenate(ks), np.concatenate(vs)
+        for h in range(num_qo_heads):
+            kh = h // group
+            if len(kc):
+                o[row, h], lse[row, h] = direct_state(scale * (kc[:, kh, :] @ q[row, h]),
+                                                      vc[:, kh, :])
+            else:
+                o[row, h], lse[row, h] = np.zeros(head_dim), -math.inf
     return o, lse
 
 

@@ -130,12 +130,19 @@ def fill_pool(rng, kv_lens, kv_indptr, kv_indices, page_size, pool_pages, hk, d,
     shape = (pool_pages, page_size, hk, d) if layout == NHD else (pool_pages, hk, page_size, d)
     k = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
     v = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
+    fill_pages(rng, k, v, kv_lens, kv_indptr, kv_indices, page_size, layout)
+    return k, v
+
+
+def fill_pages(rng, k, v, kv_lens, kv_indptr, kv_indices, page_size, layout):
+    """Write N(0,1) bf16 rows into the slots of each request's pages, in place."""
     for r, n in enumerate(np.asarray(kv_lens)):
         n = int(n)
         if n == 0:
             continue
-        rows_k = normal_bf16_bits(rng, (n, hk, d))
-        rows_v = normal_bf16_bits(rng, (n, hk, d))
+        rows_k = normal_bf16_bits(rng, (n,) + k.shape[-2:] if layout == NHD else
+                                  (n, k.shape[1], k.shape[3]))
+        rows_v = normal_bf16_bits(rng, rows_k.shape)
         pages = kv_indices[kv_indptr[r]:kv_indptr[r + 1]]
         for j0 in range(0, n, page_size):
             pg = int(pages[j0 // page_size])
@@ -146,7 +153,6 @@ def fill_pool(rng, kv_lens, kv_indptr, kv_indices, page_size, pool_pages, hk, d,
             else:
                 k[pg, :, :cnt] = rows_k[j0:j0 + cnt].transpose(1, 0, 2)
                 v[pg, :, :cnt] = rows_v[j0:j0 + cnt].transpose(1, 0, 2)
-    return k, v
 
 
 def make_paged_batch(seed, qo_lens, kv_lens, *, page_size, layout=NHD, hq=32, hk=8, d=128,
@@ -219,6 +225,81 @@ def make_ragged_batch(seed, lens, *, hq=32, hk=32, d=128, mask_mode="custom", p_
             parts.append(keep.reshape(-1))
         b.mask_bool = (np.concatenate(parts) if parts else np.zeros(0, bool)).astype(np.uint8)
     return b
+
+
+@dataclass
+class Cascade:
+    """Multi-level cascade batch: every level splits the same query rows into
+    nodes with their own page lists in one pool ("KV-Cache layouts",
+    "Multi-level cascade inference data layout").  ``levels`` runs from the
+    root; each entry holds int32 qo_indptr, kv_indptr, kv_indices,
+    last_page_len and kv_lens.  A node without keys has no pages (its
+    last_page_len is 1 and unused)."""
+
+    name: str
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    layout: str
+    mask_mode: str
+    qo_lens: np.ndarray
+    levels: list
+    q: np.ndarray | None = None
+    k_pool: np.ndarray | None = None
+    v_pool: np.ndarray | None = None
+
+    @property
+    def nnz_q(self) -> int:
+        return int(self.levels[-1]["qo_indptr"][-1])
+
+    @property
+    def kv_indices(self) -> np.ndarray:
+        """Page ids of all levels, concatenated in level order."""
+        return np.concatenate([lv["kv_indices"] for lv in self.levels]).astype(np.int32)
+
+
+def make_cascade_batch(seed, qo_lens, own_kv_lens, shared, *, page_size, layout=NHD, hq=32,
+                       hk=8, d=128, mask_mode="causal", with_payload=True, name="cascade"):
+    """Cascade over requests with query lengths ``qo_lens`` and own (last-level)
+    KV lengths ``own_kv_lens``.  ``shared`` lists the levels above the last,
+    root first; each is a list of (requests, kv_len) nodes that partition the
+    requests in order.  Page ids are a seeded permutation of a pool with
+    exactly the pages needed, consumed level by level; unused slots hold NaN."""
+    rng = np.random.default_rng(seed)
+    qo_lens = np.asarray(qo_lens, dtype=np.int64)
+    q_ptr = _prefix(qo_lens)
+    specs = []
+    for nodes in shared:
+        counts = [int(c) for c, _ in nodes]
+        assert sum(counts) == len(qo_lens), "shared nodes must partition the requests"
+        bounds = np.concatenate([[0], np.cumsum(counts)])
+        node_qo = [int(q_ptr[bounds[i + 1]] - q_ptr[bounds[i]]) for i in range(len(nodes))]
+        specs.append((np.asarray(node_qo), np.asarray([int(k) for _, k in nodes])))
+    specs.append((qo_lens, np.asarray(own_kv_lens, dtype=np.int64)))
+    pages = [(kv + page_size - 1) // page_size for _, kv in specs]
+    total = int(sum(int(p.sum()) for p in pages))
+    ids = rng.permutation(total).astype(np.int32)
+    levels, used = [], 0
+    for (qo, kv), pg in zip(specs, pages):
+        n_pages = int(pg.sum())
+        last = np.where(kv > 0, kv - (pg - 1) * page_size, 1).astype(np.int32)
+        levels.append(dict(qo_indptr=_prefix(qo), kv_indptr=_prefix(pg),
+                           kv_indices=ids[used:used + n_pages].copy(), last_page_len=last,
+                           kv_lens=kv.astype(np.int32)))
+        used += n_pages
+    c = Cascade(name=name, num_qo_heads=hq, num_kv_heads=hk, head_dim=d, page_size=page_size,
+                layout=layout, mask_mode=mask_mode, qo_lens=qo_lens.astype(np.int32),
+                levels=levels)
+    if with_payload:
+        c.q = normal_bf16_bits(rng, (int(q_ptr[-1]), hq, d))
+        shape = (total, page_size, hk, d) if layout == NHD else (total, hk, page_size, d)
+        c.k_pool = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
+        c.v_pool = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
+        for lv in levels:
+            fill_pages(rng, c.k_pool, c.v_pool, lv["kv_lens"], lv["kv_indptr"], lv["kv_indices"],
+                       page_size, layout)
+    return c
 
 
 # ---------------------------------------------------------------------------

@@ -160,6 +160,37 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* params, int32_t batch,
                     const int32_t* last_page_len_h, void* int_ws_d, size_t int_ws_bytes,
                     void* pinned_h, size_t pinned_bytes, void* stream);
 
+/* Multi-level cascade plan ("KV-Cache layouts", "Multi-level cascade
+ * inference data layout"; "Deep Dive - FlashInfer", "Core mechanism": the
+ * (o, lse) state composes across shared prefixes).
+ *   Level l (0 = root, num_levels - 1 = last) has num_nodes[l] nodes with its
+ *   own host arrays qo_indptr[l] [num_nodes[l] + 1], kv_indptr[l]
+ *   [num_nodes[l] + 1] and last_page_len[l] [num_nodes[l]], with the meaning
+ *   they have in pka_plan.  Every level splits the same query rows
+ *   (qo_indptr[l][num_nodes[l]] equal for all l).  A row attends to the keys
+ *   of the node holding it at every level: all of them at the levels above
+ *   the last (a shared prefix lies before the row's own tokens), and at the
+ *   last level those params->mask_mode leaves visible, with that node's
+ *   (qo_len, kv_len).  A node above the last may have no pages (its
+ *   last_page_len is then ignored); last-level nodes follow pka_plan's
+ *   contract.
+ *   pka_run then takes as kv_indices the page ids of all levels concatenated
+ *   in level order: level l's kv_indptr indexes its own part, which starts
+ *   after the sum of kv_indptr[l'][num_nodes[l']] over l' < l.  Each level's
+ *   work writes fp32 partial states to the float workspace and the merge
+ *   kernel combines every row's states into O and LSE in the same pka_run.
+ *   Supported: paged K/V, mask none or causal, split off/auto/fixed, up to
+ *   PKA_MAX_CASCADE_LEVELS levels; ragged K/V, custom masks and graph mode
+ *   return PKA_ERR_UNSUPPORTED.  Workspace rules and errors as in pka_plan;
+ *   rows split differently between levels give PKA_ERR_METADATA. */
+#define PKA_MAX_CASCADE_LEVELS 16
+pka_status pka_plan_cascade(pka_plan_t plan, const pka_params* params, int32_t num_levels,
+                            const int32_t* num_nodes, const int32_t* const* qo_indptr_h,
+                            const int32_t* const* kv_indptr_h,
+                            const int32_t* const* last_page_len_h, void* int_ws_d,
+                            size_t int_ws_bytes, void* pinned_h, size_t pinned_bytes,
+                            void* stream);
+
 /* Copy the plan's summary into *info. */
 pka_status pka_plan_get_info(pka_plan_t plan, pka_plan_info* info);
 

@@ -13,7 +13,8 @@ from . import _pka
 from ._pka import (PKA_HND, PKA_MASK_CAUSAL, PKA_MASK_CUSTOM, PKA_MASK_NONE, PKA_NHD,  # noqa
                    PKA_SPLIT_AUTO, PKA_SPLIT_FIXED, PKA_SPLIT_OFF, PkaError, make_params,
                    pka_append_paged_kv_cache, pka_get_device_error, pka_last_error, pka_merge_states,
-                   pka_packbits, pka_plan, pka_plan_create, pka_plan_destroy, pka_plan_get_info,
+                   pka_packbits, pka_plan, pka_plan_cascade, pka_plan_create, pka_plan_destroy,
+                   pka_plan_get_info,
                    pka_plan_wait, pka_run, pka_run_static_scratch, pka_status_str, pka_validate, pka_version)
 
 __all__ = ["BatchAttention", "make_params", "PkaError"] + [n for n in _pka.EXPORTED]
@@ -47,21 +48,35 @@ class BatchAttention:
         params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, layout, mask_mode,
                              sm_scale, kv_ragged, split_mode, fixed_split_pages, num_sms,
                              graph_max_batch, graph_max_qo_rows, graph_max_kv_tokens)
-        s = pka_plan(self.handle, params, qo_indptr, kv_indptr, last_page_len, self.int_ws,
-                     self.pinned, stream, check=False)
+        return self._plan(params, "pka_plan", lambda: pka_plan(
+            self.handle, params, qo_indptr, kv_indptr, last_page_len, self.int_ws, self.pinned,
+            stream, check=False))
+
+    def plan_cascade(self, levels, *, num_qo_heads, num_kv_heads, head_dim, page_size=1,
+                     layout="NHD", mask_mode="causal", sm_scale=0.0, split_mode="auto",
+                     fixed_split_pages=1, num_sms=0, stream=None):
+        """Multi-level cascade: ``levels`` lists, root first, each level's
+        (qo_indptr, kv_indptr, last_page_len); run() then takes the levels'
+        page ids concatenated in level order as kv_indices."""
+        params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, layout, mask_mode,
+                             sm_scale, False, split_mode, fixed_split_pages, num_sms)
+        return self._plan(params, "pka_plan_cascade", lambda: pka_plan_cascade(
+            self.handle, params, levels, self.int_ws, self.pinned, stream, check=False))
+
+    def _plan(self, params, where, call):
+        s = call()
         if s == _WORKSPACE:
             info = pka_plan_get_info(self.handle)
             pka_plan_wait(self.handle)
             if info.int_ws_bytes <= min(self.int_ws.numel(), self.pinned.numel()):
                 # not a buffer size: the batch exceeds the graph-mode capacities
-                raise PkaError(s, "pka_plan: " + pka_last_error())
+                raise PkaError(s, where + ": " + pka_last_error())
             n = max(int(info.int_ws_bytes), self.int_ws.numel())
             self.int_ws = torch.empty(n, dtype=torch.uint8, device=self.device)
             self.pinned = torch.empty(n, dtype=torch.uint8, pin_memory=True)
-            s = pka_plan(self.handle, params, qo_indptr, kv_indptr, last_page_len, self.int_ws,
-                         self.pinned, stream, check=False)
+            s = call()
         if s != 0:
-            raise PkaError(s, "pka_plan")
+            raise PkaError(s, where)
         self.params = params
         self.info = pka_plan_get_info(self.handle)
         if self.info.float_ws_bytes > self.float_ws.numel():

@@ -27,7 +27,8 @@ STATUS = {0: "PKA_OK", 1: "PKA_ERR_INVALID_ARG", 2: "PKA_ERR_METADATA", 3: "PKA_
 EXPORTED = ["pka_status_str", "pka_version", "pka_validate", "pka_plan_create",
             "pka_plan_destroy", "pka_plan", "pka_plan_get_info", "pka_plan_wait", "pka_run",
             "pka_append_paged_kv_cache", "pka_merge_states", "pka_packbits",
-            "pka_get_device_error", "pka_last_error", "pka_run_static_scratch"]
+            "pka_get_device_error", "pka_last_error", "pka_run_static_scratch",
+            "pka_plan_cascade"]
 
 
 class pka_params(ctypes.Structure):
@@ -87,6 +88,8 @@ def lib():
         L.pka_plan_destroy.argtypes = [vp]
         L.pka_plan_destroy.restype = None
         L.pka_plan.argtypes = [vp, P(pka_params), i32, vp, vp, vp, vp, sz, vp, sz, vp]
+        L.pka_plan_cascade.argtypes = [vp, P(pka_params), i32, vp, vp, vp, vp, vp, sz, vp, sz,
+                                       vp]
         L.pka_plan_get_info.argtypes = [vp, P(pka_plan_info)]
         L.pka_plan_wait.argtypes = [vp]
         L.pka_run.argtypes = [vp, P(pka_params), vp, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]
@@ -242,6 +245,29 @@ def pka_plan(handle, params, qo_indptr, kv_indptr, last_page_len, int_ws, pinned
                        ws_ptr, ws_bytes, _ptr(pinned), pin_bytes, st)
     if check:
         _check(s, "pka_plan")
+    return s
+
+
+def pka_plan_cascade(handle, params, levels, int_ws, pinned, stream=None, check=True) -> int:
+    """``levels``: list, root first, of (qo_indptr, kv_indptr, last_page_len) host int32."""
+    arrs = [tuple(_int32_host(a, n) for a, n in zip(lv, ("qo_indptr", "kv_indptr",
+                                                          "last_page_len")))
+            for lv in levels]
+    n = len(arrs)
+    nodes = np.asarray([len(a[1]) - 1 for a in arrs], dtype=np.int32)
+    ptrs = [(ctypes.c_void_p * max(n, 1))(*[_ptr(a[i]) for a in arrs]) for i in range(3)]
+    ws_ptr = _ptr(int_ws) if int_ws is not None else None
+    ws_bytes = int_ws.numel() * int_ws.element_size() if int_ws is not None else 0
+    pin_bytes = (pinned.numel() * pinned.element_size() if isinstance(pinned, torch.Tensor)
+                 else pinned.nbytes)
+    st = _stream(stream) if int_ws is not None else None
+    s = lib().pka_plan_cascade(handle, ctypes.byref(params), n, _ptr(nodes),
+                               ctypes.cast(ptrs[0], ctypes.c_void_p),
+                               ctypes.cast(ptrs[1], ctypes.c_void_p),
+                               ctypes.cast(ptrs[2], ctypes.c_void_p), ws_ptr, ws_bytes,
+                               _ptr(pinned), pin_bytes, st)
+    if check:
+        _check(s, "pka_plan_cascade")
     return s
 
 

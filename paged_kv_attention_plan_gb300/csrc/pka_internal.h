@@ -37,6 +37,7 @@ struct MergeArgs {
   const PkaMergeTask* tasks;  // plan merge list (tasks == null -> indptr mode)
   int32_t num_tasks;          // tasks, or the list's capacity when num_tasks_dev is set
   const int32_t* num_tasks_dev;  // graph mode: the task count in the device plan image
+  const int32_t* slots;       // record lists of tasks with rec_stride == 0 (cascade)
   const int32_t* indptr;      // merge_states mode: [rows + 1]
   int32_t rows;
   int32_t heads;

@@ -3,7 +3,7 @@
 // host planner and the kernels (both are the product path).
 //
 // image := header | decode_cta_ptr | decode_items | prefill_cta_ptr |
-//          prefill_items | merge_tasks          (all offsets in int32 units)
+//          prefill_items | merge_tasks | merge_slots   (offsets in int32 units)
 #pragma once
 #include <stdint.h>
 
@@ -25,7 +25,7 @@ struct PkaImageHeader {
   int32_t off_merge_tasks;       // PkaMergeTask[num_merge_tasks]
   int32_t decode_heads_per_cta;  // kv heads one decode CTA covers
   int32_t graph_mode;            // 1: fixed layout sized by the graph capacities
-  int32_t reserved;
+  int32_t off_merge_slots;       // int32[num_partial_records] record lists, 0 if none
 };
 
 // One unit of attention work: a block of kv heads (decode) or one kv head
@@ -50,7 +50,8 @@ struct PkaWorkItem {
 };
 
 // One (query row, qo head) whose partial states are merged after a split.
-// Record k (0 <= k < nslots) of the task is rec_first + k * rec_stride.
+// Record k (0 <= k < nslots) of the task is rec_first + k * rec_stride, or,
+// with rec_stride == 0 (cascade plans), merge_slots[rec_first + k].
 struct PkaMergeTask {
   int32_t out_row;
   int32_t head;
@@ -59,6 +60,9 @@ struct PkaMergeTask {
   int32_t rec_stride;
   int32_t reserved[3];
 };
+
+// Item flags
+#define PKA_ITEM_ALL_VISIBLE 1  // every key of the range is visible (cascade levels above the last)
 
 static_assert(sizeof(PkaImageHeader) == 64, "header size");
 static_assert(sizeof(PkaWorkItem) == 64, "work item size");

@@ -105,12 +105,18 @@ struct Batch {
   std::vector<int64_t> mask_base;
   int64_t total_kv = 0;
   int32_t nnz_q = 0;
+  int mask_mode = PKA_MASK_NONE;  // the mask this batch (or cascade level) applies
+  int32_t item_flags = 0;         // PkaWorkItem.flags of its items
 };
 
 // Length contract of "Why inference attention becomes irregular" and the
 // "Page table layout" section: K = P * (pages - 1) + last, 1 <= last <= P.
+// A cascade level above the last (`shared`) may hold nodes without pages; its
+// page ids sit at kv_off in the concatenated index array.
 pka_status derive(const pka_params* p, int32_t batch, const int32_t* qo, const int32_t* kv,
-                  const int32_t* last, Batch* b) {
+                  const int32_t* last, Batch* b, int mask_mode, bool shared = false,
+                  int64_t kv_off = 0) {
+  b->mask_mode = mask_mode;
   if (batch < 0 || !kv || (!p->kv_ragged && !last)) return PKA_ERR_INVALID_ARG;
   if (kv[0] != 0) return PKA_ERR_METADATA;
   if (qo && qo[0] != 0) return PKA_ERR_METADATA;
@@ -127,6 +133,8 @@ pka_status derive(const pka_params* p, int32_t batch, const int32_t* qo, const i
     int64_t klen;
     if (p->kv_ragged) {
       klen = npages;
+    } else if (npages == 0 && shared) {
+      klen = 0;
     } else {
       if (npages < 1) return PKA_ERR_METADATA;
       if (last[r] < 1 || last[r] > p->page_size) return PKA_ERR_METADATA;
@@ -135,11 +143,12 @@ pka_status derive(const pka_params* p, int32_t batch, const int32_t* qo, const i
     if (klen > INT32_MAX) return PKA_ERR_UNSUPPORTED;
     int64_t qlen = qo ? (int64_t)qo[r + 1] - qo[r] : 1;
     if (qlen < 0) return PKA_ERR_METADATA;
-    if (p->mask_mode == PKA_MASK_CAUSAL && klen < qlen) return PKA_ERR_METADATA;
+    if (mask_mode == PKA_MASK_CAUSAL && klen < qlen) return PKA_ERR_METADATA;
+    if (kv_off + kv[r] > INT32_MAX) return PKA_ERR_UNSUPPORTED;
     b->qo_len[r] = (int32_t)qlen;
     b->kv_len[r] = (int32_t)klen;
     b->q_row0[r] = (int32_t)(qo ? qo[r] : r);
-    b->kv_base[r] = kv[r];
+    b->kv_base[r] = (int32_t)(kv_off + kv[r]);
     b->total_kv += klen;
     rows += qlen;
     if (rows > INT32_MAX) return PKA_ERR_UNSUPPORTED;
@@ -166,6 +175,7 @@ PkaWorkItem make_item(const Batch& b, int r, int kv_head0, int n_kv_heads, int q
   it.out_rec = -1;
   it.mask_lo = (int32_t)(uint32_t)(b.mask_base[r] & 0xffffffffu);
   it.mask_hi = (int32_t)(b.mask_base[r] >> 32);
+  it.flags = b.item_flags;
   return it;
 }
 
@@ -177,6 +187,12 @@ struct PlanLists {
   std::vector<PkaMergeTask> merges;
   int32_t records = 0;
   int32_t decode_chunk = 0;
+  // Cascade: every piece writes partial records and each (row, head) merges
+  // the records of all levels, listed in merge_slots.
+  bool cascade = false;
+  struct Slot { int32_t row, head, rec; };
+  std::vector<Slot> slots;
+  std::vector<int32_t> merge_slots;
 };
 
 // Give the pieces of one split unit their partial records and merge tasks.
@@ -185,10 +201,18 @@ struct PlanLists {
 void assign_records(PlanLists* L, std::vector<PkaWorkItem>& items,
                     const std::vector<int>& pieces, int q_row0, int q_count, int head0,
                     int heads_total) {
-  if (pieces.size() < 2) return;
+  if (pieces.size() < 2 && !L->cascade) return;
   int per = q_count * heads_total;
   int base = L->records;
   for (size_t k = 0; k < pieces.size(); ++k) items[pieces[k]].out_rec = base + (int)k * per;
+  L->records += (int)pieces.size() * per;
+  if (L->cascade) {
+    for (size_t k = 0; k < pieces.size(); ++k)
+      for (int i = 0; i < q_count; ++i)
+        for (int h = 0; h < heads_total; ++h)
+          L->slots.push_back({q_row0 + i, head0 + h, base + (int)k * per + i * heads_total + h});
+    return;
+  }
   for (int i = 0; i < q_count; ++i)
     for (int h = 0; h < heads_total; ++h) {
       PkaMergeTask t{};
@@ -199,24 +223,50 @@ void assign_records(PlanLists* L, std::vector<PkaWorkItem>& items,
       t.rec_stride = per;
       L->merges.push_back(t);
     }
-  L->records += (int)pieces.size() * per;
+}
+
+// Cascade: one merge task per (row, head) over the records of every level,
+// listed contiguously in merge_slots (a counting sort by row and head).
+void build_slot_merges(PlanLists* L, int32_t nnz, int32_t heads) {
+  const int64_t keys = (int64_t)nnz * heads;
+  std::vector<int32_t> start(keys + 1, 0);
+  for (const auto& s : L->slots) ++start[(int64_t)s.row * heads + s.head + 1];
+  for (int64_t k = 0; k < keys; ++k) start[k + 1] += start[k];
+  L->merge_slots.assign(L->slots.size(), 0);
+  std::vector<int32_t> pos(start.begin(), start.end() - 1);
+  for (const auto& s : L->slots) L->merge_slots[pos[(int64_t)s.row * heads + s.head]++] = s.rec;
+  for (int64_t k = 0; k < keys; ++k) {
+    if (start[k + 1] == start[k]) continue;
+    PkaMergeTask t{};
+    t.out_row = (int32_t)(k / heads);
+    t.head = (int32_t)(k % heads);
+    t.rec_first = start[k];
+    t.nslots = start[k + 1] - start[k];
+    t.rec_stride = 0;  // list mode
+    L->merges.push_back(t);
+  }
 }
 
 // Decode rows (qo_len == 1): units are (request, block of kv heads); with
 // split AUTO the keys of all units are dealt out in equal shares to one
 // persistent CTA per SM (a unit may span CTAs, a CTA may hold several units).
-void plan_decode(const pka_params* p, const Batch& b, int num_sms, PlanLists* L) {
+// The units of every cascade level go into one list (a plain batch is one level).
+void plan_decode(const pka_params* p, const std::vector<Batch>& lv, int num_sms, PlanLists* L) {
   int g = p->num_qo_heads / p->num_kv_heads;
   int hpc = pka::decode_heads_per_cta(p->num_kv_heads, g);
   int hg_count = p->num_kv_heads / hpc;
-  struct Unit { int r, hg, K; };
+  struct Unit { int l, r, hg, K; };
   std::vector<Unit> units;
   int64_t total = 0;
-  for (int r = 0; r < (int)b.qo_len.size(); ++r) {
-    if (b.qo_len[r] != 1) continue;
-    for (int hg = 0; hg < hg_count; ++hg) {
-      units.push_back({r, hg, b.kv_len[r]});
-      total += b.kv_len[r];
+  for (int l = 0; l < (int)lv.size(); ++l) {
+    const Batch& b = lv[l];
+    for (int r = 0; r < (int)b.qo_len.size(); ++r) {
+      if (b.qo_len[r] != 1) continue;
+      if (L->cascade && b.kv_len[r] == 0) continue;  // an empty node adds no state
+      for (int hg = 0; hg < hg_count; ++hg) {
+        units.push_back({l, r, hg, b.kv_len[r]});
+        total += b.kv_len[r];
+      }
     }
   }
   if (units.empty()) return;
@@ -239,11 +289,11 @@ void plan_decode(const pka_params* p, const Batch& b, int num_sms, PlanLists* L)
       do {
         int64_t t1 = std::min<int64_t>(u.K, t + step);
         pieces.push_back((int)items.size());
-        items.push_back(make_item(b, u.r, u.hg * hpc, hpc, 0, 1, (int)t, (int)t1));
+        items.push_back(make_item(lv[u.l], u.r, u.hg * hpc, hpc, 0, 1, (int)t, (int)t1));
         L->dec_cta_ptr.push_back((int)items.size());
         t = t1;
       } while (t < u.K);
-      assign_records(L, items, pieces, b.q_row0[u.r], 1, u.hg * hpc * g, hpc * g);
+      assign_records(L, items, pieces, lv[u.l].q_row0[u.r], 1, u.hg * hpc * g, hpc * g);
     }
     return;
   }
@@ -264,7 +314,7 @@ void plan_decode(const pka_params* p, const Batch& b, int num_sms, PlanLists* L)
         }
       }
       pieces.push_back((int)items.size());
-      items.push_back(make_item(b, u.r, u.hg * hpc, hpc, 0, 1, (int)t, (int)(t + take)));
+      items.push_back(make_item(lv[u.l], u.r, u.hg * hpc, hpc, 0, 1, (int)t, (int)(t + take)));
       t += take;
       load += take;
       if (load >= chunk) {
@@ -272,7 +322,7 @@ void plan_decode(const pka_params* p, const Batch& b, int num_sms, PlanLists* L)
         load = 0;
       }
     } while (t < u.K);
-    assign_records(L, items, pieces, b.q_row0[u.r], 1, u.hg * hpc * g, hpc * g);
+    assign_records(L, items, pieces, lv[u.l].q_row0[u.r], 1, u.hg * hpc * g, hpc * g);
   }
   if (L->dec_cta_ptr.back() != (int)items.size()) L->dec_cta_ptr.push_back((int)items.size());
 }
@@ -282,23 +332,27 @@ void plan_decode(const pka_params* p, const Batch& b, int num_sms, PlanLists* L)
 // pack with the tokens into two 128-row tiles that share every K/V load.  Causal
 // units only visit keys up to the tile's last visible one.  Items are dealt
 // to CTAs longest-first onto the least loaded CTA.
-void plan_prefill(const pka_params* p, const Batch& b, int num_sms, PlanLists* L) {
+void plan_prefill(const pka_params* p, const std::vector<Batch>& lv, int num_sms, PlanLists* L) {
   int g = p->num_qo_heads / p->num_kv_heads;
   int tq = 2 * (pka::kPrefillTileRows / g);
-  struct Unit { int r, h, q0, qc, kend; };
+  struct Unit { int l, r, h, q0, qc, kend; };
   std::vector<Unit> units;
   int64_t total_tiles = 0;
-  for (int r = 0; r < (int)b.qo_len.size(); ++r) {
-    int Q = b.qo_len[r], K = b.kv_len[r];
-    if (Q < 2) continue;
-    for (int h = 0; h < p->num_kv_heads; ++h)
-      for (int q0 = 0; q0 < Q; q0 += tq) {
-        int qc = std::min(tq, Q - q0);
-        int kend = K;
-        if (p->mask_mode == PKA_MASK_CAUSAL) kend = K - Q + (q0 + qc - 1) + 1;
-        units.push_back({r, h, q0, qc, kend});
-        total_tiles += (kend + pka::kPrefillTileKeys - 1) / pka::kPrefillTileKeys;
-      }
+  for (int l = 0; l < (int)lv.size(); ++l) {
+    const Batch& b = lv[l];
+    for (int r = 0; r < (int)b.qo_len.size(); ++r) {
+      int Q = b.qo_len[r], K = b.kv_len[r];
+      if (Q < 2) continue;
+      if (L->cascade && K == 0) continue;  // an empty node adds no state
+      for (int h = 0; h < p->num_kv_heads; ++h)
+        for (int q0 = 0; q0 < Q; q0 += tq) {
+          int qc = std::min(tq, Q - q0);
+          int kend = K;
+          if (b.mask_mode == PKA_MASK_CAUSAL) kend = K - Q + (q0 + qc - 1) + 1;
+          units.push_back({l, r, h, q0, qc, kend});
+          total_tiles += (kend + pka::kPrefillTileKeys - 1) / pka::kPrefillTileKeys;
+        }
+    }
   }
   if (units.empty()) return;
   int64_t chunk = 0;  // keys per piece, 0 = whole range
@@ -318,11 +372,11 @@ void plan_prefill(const pka_params* p, const Batch& b, int num_sms, PlanLists* L
     do {
       int64_t t1 = std::min<int64_t>(u.kend, t + step);
       pieces.push_back((int)items.size());
-      items.push_back(make_item(b, u.r, u.h, 1, u.q0, u.qc, (int)t, (int)t1));
+      items.push_back(make_item(lv[u.l], u.r, u.h, 1, u.q0, u.qc, (int)t, (int)t1));
       cost.push_back((t1 - t) + 64);
       t = t1;
     } while (t < u.kend);
-    assign_records(L, items, pieces, b.q_row0[u.r] + u.q0, u.qc, u.h * g, g);
+    assign_records(L, items, pieces, lv[u.l].q_row0[u.r] + u.q0, u.qc, u.h * g, g);
   }
   int n = (int)items.size();
   int ctas = std::min(n, num_sms);
@@ -392,65 +446,15 @@ void pka::set_last_error(const char* msg) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
 }
 
-extern "C" {
+namespace {
 
-const char* pka_status_str(pka_status s) {
-  switch (s) {
-    case PKA_OK: return "ok";
-    case PKA_ERR_INVALID_ARG: return "invalid argument";
-    case PKA_ERR_METADATA: return "metadata violates the indptr / page-table contract";
-    case PKA_ERR_UNSUPPORTED: return "unsupported head_dim, head ratio or mode";
-    case PKA_ERR_WORKSPACE: return "workspace or staging buffer too small";
-    case PKA_ERR_STALE_PLAN: return "run parameters differ from the planned ones";
-    case PKA_ERR_CUDA: return "CUDA runtime error";
-    case PKA_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on a barrier";
-  }
-  return "unknown status";
-}
-
-pka_status pka_version(int32_t* major, int32_t* minor) {
-  if (!major || !minor) return PKA_ERR_INVALID_ARG;
-  *major = PKA_VERSION_MAJOR;
-  *minor = PKA_VERSION_MINOR;
-  return PKA_OK;
-}
-
-pka_status pka_validate(const pka_params* p, int32_t batch, const int32_t* qo,
-                        const int32_t* kv, const int32_t* last) {
-  if (!params_ok(p)) return PKA_ERR_INVALID_ARG;
-  pka_status s = check_supported(p);
-  if (s != PKA_OK) return s;
-  Batch b;
-  return derive(p, batch, qo, kv, last, &b);
-}
-
-pka_status pka_plan_create(pka_plan_t* plan) {
-  if (!plan) return PKA_ERR_INVALID_ARG;
-  *plan = new (std::nothrow) pka_plan_s();
-  return *plan ? PKA_OK : PKA_ERR_INVALID_ARG;
-}
-
-void pka_plan_destroy(pka_plan_t plan) {
-  if (!plan) return;
-  if (plan->event) {
-    cudaEventSynchronize(plan->event);
-    cudaEventDestroy(plan->event);
-  }
-  delete plan;
-}
-
-pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const int32_t* qo,
-                    const int32_t* kv, const int32_t* last, void* int_ws_d, size_t int_ws_bytes,
-                    void* pinned_h, size_t pinned_bytes, void* stream) {
-  if (!plan || !params_ok(p)) return PKA_ERR_INVALID_ARG;
-  plan->planned = false;
-  plan->info = pka_plan_info{};
-  pka_status s = check_supported(p);
-  if (s != PKA_OK) return s;
-  Batch b;
-  s = derive(p, batch, qo, kv, last, &b);
-  if (s != PKA_OK) return s;
-
+// Plan the levels (one for a plain batch) into the image and start its copy.
+pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<Batch>& lv,
+                       int32_t batch, bool cascade, void* int_ws_d, size_t int_ws_bytes,
+                       void* pinned_h, size_t pinned_bytes, void* stream) {
+  const int32_t nnz = lv.back().nnz_q;
+  int64_t total_kv = 0;
+  for (const Batch& b : lv) total_kv += b.total_kv;
   int num_sms = p->num_sms;
   if (num_sms == 0) {
     if (int_ws_d) {
@@ -464,15 +468,17 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   }
 
   const bool graph = graph_mode(p);
-  if (graph && (batch > p->graph_max_batch || b.nnz_q > p->graph_max_qo_rows ||
-                (p->kv_ragged && b.total_kv > p->graph_max_kv_tokens))) {
+  if (graph && (batch > p->graph_max_batch || nnz > p->graph_max_qo_rows ||
+                (p->kv_ragged && total_kv > p->graph_max_kv_tokens))) {
     pka::set_last_error("batch exceeds the graph-mode capacities");
     return PKA_ERR_WORKSPACE;
   }
 
   PlanLists L;
-  plan_decode(p, b, num_sms, &L);
-  plan_prefill(p, b, num_sms, &L);
+  L.cascade = cascade;
+  plan_decode(p, lv, num_sms, &L);
+  plan_prefill(p, lv, num_sms, &L);
+  if (cascade) build_slot_merges(&L, nnz, p->num_qo_heads);
   GraphCaps caps;
   if (graph) {
     caps = graph_caps(p, num_sms);
@@ -515,6 +521,8 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   w = align_words(w + n_pre * kItemWords);
   h.off_merge_tasks = (int)w;
   w = align_words(w + n_merge * kMergeWords);
+  h.off_merge_slots = L.merge_slots.empty() ? 0 : (int)w;
+  w = align_words(w + L.merge_slots.size());
   if (w > (size_t)INT32_MAX || layout_records > INT32_MAX / 256) {
     pka::set_last_error("plan image or partial records exceed 2^31");
     return PKA_ERR_UNSUPPORTED;
@@ -528,8 +536,8 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   info.float_ws_bytes =
       layout_records ? rec_o_al + (((size_t)layout_records * 4 + 255) & ~size_t(255)) : 0;
   info.num_requests = batch;
-  info.nnz_qo = b.nnz_q;
-  info.total_kv = b.total_kv;
+  info.nnz_qo = nnz;
+  info.total_kv = total_kv;
   info.num_decode_ctas = h.num_decode_ctas;
   info.num_decode_items = h.num_decode_items;
   info.num_prefill_ctas = h.num_prefill_ctas;
@@ -569,6 +577,8 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
     std::memcpy(img + h.off_prefill_items, L.pre_items.data(), L.pre_items.size() * sizeof(PkaWorkItem));
   if (!L.merges.empty())
     std::memcpy(img + h.off_merge_tasks, L.merges.data(), L.merges.size() * sizeof(PkaMergeTask));
+  if (!L.merge_slots.empty())
+    std::memcpy(img + h.off_merge_slots, L.merge_slots.data(), L.merge_slots.size() * 4);
 
   plan->params = *p;
   plan->hdr = h;
@@ -589,6 +599,100 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   }
   plan->planned = true;
   return PKA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pka_status_str(pka_status s) {
+  switch (s) {
+    case PKA_OK: return "ok";
+    case PKA_ERR_INVALID_ARG: return "invalid argument";
+    case PKA_ERR_METADATA: return "metadata violates the indptr / page-table contract";
+    case PKA_ERR_UNSUPPORTED: return "unsupported head_dim, head ratio or mode";
+    case PKA_ERR_WORKSPACE: return "workspace or staging buffer too small";
+    case PKA_ERR_STALE_PLAN: return "run parameters differ from the planned ones";
+    case PKA_ERR_CUDA: return "CUDA runtime error";
+    case PKA_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on a barrier";
+  }
+  return "unknown status";
+}
+
+pka_status pka_version(int32_t* major, int32_t* minor) {
+  if (!major || !minor) return PKA_ERR_INVALID_ARG;
+  *major = PKA_VERSION_MAJOR;
+  *minor = PKA_VERSION_MINOR;
+  return PKA_OK;
+}
+
+pka_status pka_validate(const pka_params* p, int32_t batch, const int32_t* qo,
+                        const int32_t* kv, const int32_t* last) {
+  if (!params_ok(p)) return PKA_ERR_INVALID_ARG;
+  pka_status s = check_supported(p);
+  if (s != PKA_OK) return s;
+  Batch b;
+  return derive(p, batch, qo, kv, last, &b, p->mask_mode);
+}
+
+pka_status pka_plan_create(pka_plan_t* plan) {
+  if (!plan) return PKA_ERR_INVALID_ARG;
+  *plan = new (std::nothrow) pka_plan_s();
+  return *plan ? PKA_OK : PKA_ERR_INVALID_ARG;
+}
+
+void pka_plan_destroy(pka_plan_t plan) {
+  if (!plan) return;
+  if (plan->event) {
+    cudaEventSynchronize(plan->event);
+    cudaEventDestroy(plan->event);
+  }
+  delete plan;
+}
+
+pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const int32_t* qo,
+                    const int32_t* kv, const int32_t* last, void* int_ws_d, size_t int_ws_bytes,
+                    void* pinned_h, size_t pinned_bytes, void* stream) {
+  if (!plan || !params_ok(p)) return PKA_ERR_INVALID_ARG;
+  plan->planned = false;
+  plan->info = pka_plan_info{};
+  pka_status s = check_supported(p);
+  if (s != PKA_OK) return s;
+  std::vector<Batch> lv(1);
+  s = derive(p, batch, qo, kv, last, &lv[0], p->mask_mode);
+  if (s != PKA_OK) return s;
+  return plan_levels(plan, p, lv, batch, false, int_ws_d, int_ws_bytes, pinned_h, pinned_bytes,
+                     stream);
+}
+
+pka_status pka_plan_cascade(pka_plan_t plan, const pka_params* p, int32_t num_levels,
+                            const int32_t* num_nodes, const int32_t* const* qo,
+                            const int32_t* const* kv, const int32_t* const* last, void* int_ws_d,
+                            size_t int_ws_bytes, void* pinned_h, size_t pinned_bytes,
+                            void* stream) {
+  if (!plan || !params_ok(p)) return PKA_ERR_INVALID_ARG;
+  plan->planned = false;
+  plan->info = pka_plan_info{};
+  pka_status s = check_supported(p);
+  if (s != PKA_OK) return s;
+  if (p->kv_ragged || p->mask_mode == PKA_MASK_CUSTOM || graph_mode(p)) return PKA_ERR_UNSUPPORTED;
+  if (num_levels < 1 || num_levels > PKA_MAX_CASCADE_LEVELS || !num_nodes || !qo || !kv || !last)
+    return PKA_ERR_INVALID_ARG;
+  std::vector<Batch> lv(num_levels);
+  int64_t kv_off = 0;
+  for (int l = 0; l < num_levels; ++l) {
+    if (!qo[l] || !kv[l] || !last[l] || num_nodes[l] < 0) return PKA_ERR_INVALID_ARG;
+    const bool shared = l + 1 < num_levels;
+    s = derive(p, num_nodes[l], qo[l], kv[l], last[l], &lv[l],
+               shared ? (int)PKA_MASK_NONE : p->mask_mode, shared, kv_off);
+    if (s != PKA_OK) return s;
+    if (lv[l].nnz_q != lv[0].nnz_q) return PKA_ERR_METADATA;  // levels split the same rows
+    if (shared && p->mask_mode != PKA_MASK_NONE) lv[l].item_flags = PKA_ITEM_ALL_VISIBLE;
+    kv_off += kv[l][num_nodes[l]];
+  }
+  if (kv_off > INT32_MAX) return PKA_ERR_UNSUPPORTED;
+  return plan_levels(plan, p, lv, num_nodes[num_levels - 1], true, int_ws_d, int_ws_bytes,
+                     pinned_h, pinned_bytes, stream);
 }
 
 pka_status pka_plan_get_info(pka_plan_t plan, pka_plan_info* info) {
@@ -672,6 +776,7 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
     m.tasks = reinterpret_cast<const PkaMergeTask*>(plan->int_ws_d + h.off_merge_tasks);
     m.num_tasks = graph ? plan->merge_capacity : h.num_merge_tasks;
     if (graph) m.num_tasks_dev = plan->int_ws_d + offsetof(PkaImageHeader, num_merge_tasks) / 4;
+    if (h.off_merge_slots) m.slots = plan->int_ws_d + h.off_merge_slots;
     m.heads = p->num_qo_heads;
     m.part_o = a.part_o;
     m.part_lse = a.part_lse;

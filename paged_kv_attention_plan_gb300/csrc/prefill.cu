@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int klim = w.kv_len - w.qo_len + i;      // causal: keys <= klim are visible
       const int klim_first = w.kv_len - w.qo_len + w.q_local0 + x * TQ;
       const int64_t mrow = ((int64_t)w.mask_hi << 32 | (uint32_t)w.mask_lo) + (int64_t)i * w.kv_len;
+      const int mm = (w.flags & PKA_ITEM_ALL_VISIBLE) ? (int)PKA_MASK_NONE : a.mask_mode;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int k = 0; k < n; ++k) {
@@ -449,12 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb = w.t0 + k * BN;
         // Only tiles that reach past the key range, the causal diagonal of the
         // warpgroup's first row, or a custom mask need per-element masking.
-        const bool need_mask = (kb + BN > w.t1) || a.mask_mode == PKA_MASK_CUSTOM ||
-                               (a.mask_mode == PKA_MASK_CAUSAL && kb + BN - 1 > klim_first);
+        const bool need_mask = (kb + BN > w.t1) || mm == PKA_MASK_CUSTOM ||
+                               (mm == PKA_MASK_CAUSAL && kb + BN - 1 > klim_first);
         int vis_end = w.t1 - kb;
-        if (a.mask_mode == PKA_MASK_CAUSAL) vis_end = min(vis_end, klim - kb + 1);
+        if (mm == PKA_MASK_CAUSAL) vis_end = min(vis_end, klim - kb + 1);
         uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        if (a.mask_mode == PKA_MASK_CUSTOM)
+        if (mm == PKA_MASK_CUSTOM)
           load_mask_bits(a.mask, mrow + kb, mrow + min(w.t1, w.kv_len), mbits);
         // The whole S row in one round trip (four 32-column loads, one wait):
         // under tensor-core traffic a TMEM load takes hundreds of cycles, so

@@ -70,17 +70,21 @@ __device__ __forceinline__ void merge_one(const MergeArgs& a, const int task, co
     nslots = s1 - s0;
     stride = a.heads;
   }
+  // record of slot k: strided, or listed (stride 0)
+  auto rec_of = [&](int k) -> int64_t {
+    return stride ? (int64_t)rec_first + (int64_t)k * stride : (int64_t)a.slots[rec_first + k];
+  };
   float shift = -INFINITY;
-  for (int k = 0; k < nslots; ++k) shift = fmaxf(shift, a.part_lse[(int64_t)rec_first + (int64_t)k * stride]);
+  for (int k = 0; k < nslots; ++k) shift = fmaxf(shift, a.part_lse[rec_of(k)]);
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float z = 0.f;
   if (shift != -INFINITY) {
-    for (int k = 0; k < nslots; ++k) z += exp2f(a.part_lse[(int64_t)rec_first + (int64_t)k * stride] - shift);
+    for (int k = 0; k < nslots; ++k) z += exp2f(a.part_lse[rec_of(k)] - shift);
     const float inv_z = 1.f / z;
     for (int k = 0; k < nslots; ++k) {
-      const int64_t rec = (int64_t)rec_first + (int64_t)k * stride;
+      const int64_t rec = rec_of(k);
       const float b = a.part_lse[rec];
       if (b == -INFINITY) continue;
       const float scale = exp2f(b - shift) * inv_z;

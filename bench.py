@@ -146,6 +146,13 @@ def decode_setup(device):
     info = attn.plan(None, b.kv_indptr, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
                      head_dim=128, page_size=16, split_mode="auto")
     d["attn"], d["info"] = attn, info
+    t = []
+    for _ in range(20):  # host time of one plan() (validation, planning, image, async copy)
+        t0 = time.perf_counter()
+        attn.plan(None, b.kv_indptr, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
+                  head_dim=128, page_size=16, split_mode="auto")
+        t.append(time.perf_counter() - t0)
+    d["plan_us"] = statistics.median(t) * 1e6
     d["o"] = torch.empty_like(d["q"])
     d["lse"] = torch.empty(b.nnz_q, 32, dtype=torch.float32, device=device)
     kv_tokens = int(np.sum(b.kv_lens))
@@ -311,6 +318,63 @@ def mixed_step(d):
     d["attn"].run(d["q"], d["k"], d["v"], d["idx"], out=d["o"], lse=d["lse"])
 
 
+def cascade_setup(device):
+    """64 decode rows sharing a 32768-token prompt (own suffixes U[512,2048]),
+    planned as a two-level cascade and, for comparison, as a flat batch whose
+    page tables each list the prompt's pages."""
+    import paged_kv_attention_plan_gb300 as pka
+    from paged_kv_attention_plan_gb300 import workloads as W
+    from tests.gpu_util import i32
+
+    c = W.shared_prompt_decode(with_payload=False)
+    root, own = c.levels
+    pages = int(c.kv_indices.size)
+    g = torch.Generator(device=device).manual_seed(1005)
+    d = {}
+    d["k"] = torch.randn((pages, 16, 8, 128), generator=g, device=device).to(torch.bfloat16)
+    d["v"] = torch.randn((pages, 16, 8, 128), generator=g, device=device).to(torch.bfloat16)
+    d["q"] = torch.randn((c.nnz_q, 32, 128), generator=g, device=device).to(torch.bfloat16)
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty(c.nnz_q, 32, dtype=torch.float32, device=device)
+    d["idx"] = i32(c.kv_indices, device)
+    casc = pka.BatchAttention(device=device)
+    levels = [(lv["qo_indptr"], lv["kv_indptr"], lv["last_page_len"]) for lv in c.levels]
+    kw = dict(num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    d["info"] = casc.plan_cascade(levels, **kw)
+    d["casc"] = casc
+    t = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        casc.plan_cascade(levels, **kw)
+        t.append(time.perf_counter() - t0)
+    d["plan_us"] = statistics.median(t) * 1e6
+    kv_indptr, flat = [0], []
+    for r in range(len(own["kv_lens"])):
+        flat += list(root["kv_indices"]) + list(own["kv_indices"][own["kv_indptr"][r]:
+                                                                  own["kv_indptr"][r + 1]])
+        kv_indptr.append(len(flat))
+    flat_attn = pka.BatchAttention(device=device)
+    flat_attn.plan(None, np.asarray(kv_indptr, np.int32), own["last_page_len"], **kw)
+    d["flat"] = flat_attn
+    d["flat_idx"] = i32(np.asarray(flat, np.int32), device)
+    n, prompt = len(own["kv_lens"]), int(root["kv_lens"][0])
+    own_tokens = int(np.sum(own["kv_lens"]))
+    d["unique_bytes"] = (prompt + own_tokens) * 8 * 128 * 2 * 2
+    d["flat_bytes"] = (n * prompt + own_tokens) * 8 * 128 * 2 * 2
+    d["shared_flops"] = 4 * 128 * 32 * n * prompt
+    d["own_bytes"] = own_tokens * 8 * 128 * 2 * 2
+    d["prompt_bytes"] = prompt * 8 * 128 * 2 * 2
+    return d
+
+
+def cascade_step(d):
+    d["casc"].run(d["q"], d["k"], d["v"], d["idx"], out=d["o"], lse=d["lse"])
+
+
+def cascade_flat_step(d):
+    d["flat"].run(d["q"], d["k"], d["v"], d["flat_idx"], out=d["o"], lse=d["lse"])
+
+
 def oracle_sample(seconds_budget=20.0, max_requests=None):
     """CPU oracle on the first requests of the batch-decode workload."""
     from oracle import ref
@@ -385,6 +449,10 @@ def profile_one(name, device, stream, steps, warmup, pk):
         d = mixed_setup(device, P, "NHD" if P == 1 else "HND")
         ms = time_steps(lambda: mixed_step(d), steps, warmup, stream)
         out = {"workload": f"mixed_step_page{P}", "ms": statistics.median(ms)}
+    elif name == "cascade":
+        d = cascade_setup(device)
+        ms = time_steps(lambda: cascade_step(d), steps, warmup, stream)
+        out = {"workload": "shared_prompt_decode (cascade)", "ms": statistics.median(ms)}
     else:
         d = ragged_setup(device)
         ms = time_steps(lambda: ragged_step(d), steps, warmup, stream)
@@ -401,7 +469,7 @@ def main():
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "ragged", "mixed1",
-                                                          "mixed16"],
+                                                          "mixed16", "cascade"],
                     help="all (default) prints the benchmark line; a single workload only runs "
                          "that workload's kernels (for profiling) and prints its numbers")
     args = ap.parse_args()
@@ -509,6 +577,26 @@ def main():
                      if k in ("num_decode_ctas", "num_prefill_ctas", "num_merge_tasks")}}
         del mx
         torch.cuda.empty_cache()
+    cs = cascade_setup(device)
+    c_ms = statistics.median(time_steps(lambda: cascade_step(cs), 50, 5, stream))
+    f_ms = statistics.median(time_steps(lambda: cascade_flat_step(cs), 20, 3, stream))
+    t_roof = (cs["own_bytes"] + cs["prompt_bytes"]) / (pk["hbm_gbs"] * 1e9) + \
+        cs["shared_flops"] / (pk["bf16_tflops"] * 1e12)
+    cascade = {"workload": "shared_prompt_decode: 64 decode rows share a 32768-token prompt, own "
+                           "suffix U[512,2048] (seed 1005), page 16 NHD, 32/8 heads, D 128; "
+                           "two-level cascade plan vs flat plan listing the prompt pages per "
+                           "request",
+               "cascade_ms": c_ms, "flat_ms": f_ms, "speedup": f_ms / c_ms,
+               "flat_equiv_gbs": cs["flat_bytes"] / (c_ms * 1e-3) / 1e9,
+               "flat_gbs": cs["flat_bytes"] / (f_ms * 1e-3) / 1e9,
+               "unique_kv_bytes": cs["unique_bytes"], "shared_flops": cs["shared_flops"],
+               "roofline_ms": t_roof * 1e3, "frac_of_summed_roofline": t_roof / (c_ms * 1e-3),
+               "plan_host_us": cs["plan_us"],
+               "plan": {k: v for k, v in cs["info"].as_dict().items()
+                        if k in ("num_decode_ctas", "num_prefill_ctas", "num_prefill_items",
+                                 "num_merge_tasks", "num_partial_records")}}
+    del cs
+    torch.cuda.empty_cache()
     mixed["workload"] = ("mixed_step: 8 decodes kv U[32768,131072] + 120 decodes kv U[64,2048] + "
                          "4 chunks of 512 (prefix U[0,8192]) (seed 1003), 32/8 heads, D 128; "
                          "page 1 NHD and page 16 HND; one run() = decode + tensor-core + merge "
@@ -530,9 +618,10 @@ def main():
                        "l2": "inputs (604 MB of K/V) larger than L2; no flush",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "prefill": prefill, "ragged_custom_mask": ragged,
-            "mixed_step": mixed, "e2e": e2e,
+            "mixed_step": mixed, "cascade": cascade, "e2e": e2e,
             "gpu_launches": d["launches"] * args.steps,
-            "clocks": clocks.summary(), "plan": d["info"].as_dict()}
+            "clocks": clocks.summary(), "plan": d["info"].as_dict(),
+            "plan_host_us": d["plan_us"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, nreq, secs = oracle_sample(seconds_budget=15.0)
         line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": cpu_threads(),

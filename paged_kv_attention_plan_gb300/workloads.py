@@ -356,6 +356,18 @@ def mixed_step(seed=1003, page_size=1, layout=NHD, n_long=8, long_lo=32768, long
                             with_payload=with_payload)
 
 
+def shared_prompt_decode(seed=1005, n=64, prompt=32768, own_lo=512, own_hi=2048, page_size=16,
+                         layout=NHD, hq=32, hk=8, d=128, with_payload=True):
+    """Two-level cascade: ``n`` decode rows share a ``prompt``-token root node;
+    each request's own suffix is U[own_lo, own_hi] tokens (its newest token
+    included)."""
+    rng = np.random.default_rng(seed)
+    own = rng.integers(own_lo, own_hi, size=n, endpoint=True)
+    return make_cascade_batch(seed, np.ones(n, np.int64), own, [[(n, prompt)]],
+                              page_size=page_size, layout=layout, hq=hq, hk=hk, d=d,
+                              with_payload=with_payload, name="shared_prompt_decode")
+
+
 def ragged_custom_mask(seed=1004, n=8, lo=256, hi=2048, hq=32, hk=32, d=128, with_payload=True):
     """8 requests, qo_len == kv_len ~ U[256, 2048], ragged K/V, custom mask."""
     rng = np.random.default_rng(seed)

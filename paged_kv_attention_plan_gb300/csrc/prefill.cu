@@ -442,21 +442,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int k = 0; k < n; ++k) {
+        const int kb = w.t0 + k * BN;
+        // Custom-mask words are read before the wait on S, so that their
+        // global-memory latency overlaps the tile's MMAs.
+        uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (mm == PKA_MASK_CUSTOM)
+          load_mask_bits(a.mask, mrow + kb, mrow + min(w.t1, w.kv_len), mbits);
         if (!mbar_wait(smem_u32(&bars.s_full[x]), (uses + k) & 1)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const int kb = w.t0 + k * BN;
         // Only tiles that reach past the key range, the causal diagonal of the
-        // warpgroup's first row, or a custom mask need per-element masking.
-        const bool need_mask = (kb + BN > w.t1) || mm == PKA_MASK_CUSTOM ||
-                               (mm == PKA_MASK_CAUSAL && kb + BN - 1 > klim_first);
+        // warpgroup's first row, or a custom mask with a cleared bit in this
+        // row need per-element masking.
+        const bool need_mask =
+            (kb + BN > w.t1) ||
+            (mm == PKA_MASK_CUSTOM && (mbits[0] & mbits[1] & mbits[2] & mbits[3]) != 0xffffffffu) ||
+            (mm == PKA_MASK_CAUSAL && kb + BN - 1 > klim_first);
         int vis_end = w.t1 - kb;
         if (mm == PKA_MASK_CAUSAL) vis_end = min(vis_end, klim - kb + 1);
-        uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        if (mm == PKA_MASK_CUSTOM)
-          load_mask_bits(a.mask, mrow + kb, mrow + min(w.t1, w.kv_len), mbits);
         // The whole S row in one round trip (four 32-column loads, one wait):
         // under tensor-core traffic a TMEM load takes hundreds of cycles, so
         // one exposed latency per tile instead of one per chunk.
@@ -465,13 +470,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN / 32; ++c) tc::tmem_ld32(tS + c * 32, r[c]);
         tc::tmem_ld_wait();
         if (need_mask) {
+          // fold the end of the visible range into the bits, then one bit
+          // test per score
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            const int rem = vis_end - 32 * c;
+            if (rem <= 0) mbits[c] = 0u;
+            else if (rem < 32) mbits[c] &= (1u << rem) - 1u;
+          }
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = c * 32 + j;
-              if (!(col < vis_end && ((mbits[c] >> j) & 1u))) r[c][j] = __float_as_uint(-INFINITY);
-            }
+            for (int j = 0; j < 32; ++j)
+              if (!(mbits[c] & (1u << j))) r[c][j] = __float_as_uint(-INFINITY);
         }
         float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -545,32 +556,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_sync();
+        // All of O in one round trip; O's columns are free for the next
+        // item's PV as soon as the loads complete, before any global store.
+        uint32_t r[D / 32][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(tO + c * 32, r);
-          tc::tmem_ld_wait();
-          if (!store) continue;
-          if (w.out_rec < 0) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 v;
-              v.x = float2_to_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
-              v.y = float2_to_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-              v.z = float2_to_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
-              v.w = float2_to_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
-              *reinterpret_cast<uint4*>(odst + c * 32 + j) = v;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(pdst + c * 32 + j) =
-                  make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
-                              __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-          }
-        }
+        for (int c = 0; c < D / 32; ++c) tc::tmem_ld32(tO + c * 32, r[c]);
+        tc::tmem_ld_wait();
         tc::fence_before_sync();
         mbar_arrive(smem_u32(&bars.o_free[x]));
+        if (store) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            if (w.out_rec < 0) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                uint4 v;
+                v.x = float2_to_bf16x2(__uint_as_float(r[c][j]) * inv,
+                                       __uint_as_float(r[c][j + 1]) * inv);
+                v.y = float2_to_bf16x2(__uint_as_float(r[c][j + 2]) * inv,
+                                       __uint_as_float(r[c][j + 3]) * inv);
+                v.z = float2_to_bf16x2(__uint_as_float(r[c][j + 4]) * inv,
+                                       __uint_as_float(r[c][j + 5]) * inv);
+                v.w = float2_to_bf16x2(__uint_as_float(r[c][j + 6]) * inv,
+                                       __uint_as_float(r[c][j + 7]) * inv);
+                *reinterpret_cast<uint4*>(odst + c * 32 + j) = v;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(pdst + c * 32 + j) = make_float4(
+                    __uint_as_float(r[c][j]) * inv, __uint_as_float(r[c][j + 1]) * inv,
+                    __uint_as_float(r[c][j + 2]) * inv, __uint_as_float(r[c][j + 3]) * inv);
+            }
+          }
+        }
       } else if (store) {
         // empty key range: zero output
         for (int j = 0; j < D; j += 8) {

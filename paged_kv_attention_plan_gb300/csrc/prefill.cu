@@ -219,6 +219,17 @@ __device__ __forceinline__ void load_mask_bits(const uint8_t* mask, int64_t star
   }
 }
 
+// 32-byte global store (sm_100 family); the address must be 32-byte aligned.
+// Each thread of the epilogue writes its own row, so a warp's store touches 32
+// rows: 32-byte pieces make every piece a whole sector and halve the count.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                             uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ Maps maps, const PrefillParams pp) {
@@ -564,7 +575,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         mbar_arrive(smem_u32(&bars.o_free[x]));
-        if (store) {
+        const bool v8 =
+            ((reinterpret_cast<uintptr_t>(a.o) | reinterpret_cast<uintptr_t>(a.part_o)) & 31) == 0;
+        if (store && v8) {
+          auto cv = [&](int c, int j) {
+            return float2_to_bf16x2(__uint_as_float(r[c][j]) * inv,
+                                    __uint_as_float(r[c][j + 1]) * inv);
+          };
+          auto fv = [&](int c, int j) { return __float_as_uint(__uint_as_float(r[c][j]) * inv); };
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            if (w.out_rec < 0) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 16)
+                st_global_v8(odst + c * 32 + j, cv(c, j), cv(c, j + 2), cv(c, j + 4),
+                             cv(c, j + 6), cv(c, j + 8), cv(c, j + 10), cv(c, j + 12),
+                             cv(c, j + 14));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8)
+                st_global_v8(pdst + c * 32 + j, fv(c, j), fv(c, j + 1), fv(c, j + 2),
+                             fv(c, j + 3), fv(c, j + 4), fv(c, j + 5), fv(c, j + 6),
+                             fv(c, j + 7));
+            }
+          }
+        } else if (store) {  // 16-byte aligned outputs
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             if (w.out_rec < 0) {

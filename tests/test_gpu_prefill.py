@@ -195,3 +195,20 @@ def test_custom_mask_unaligned_buffer():
     o, lse = attn.run(bf16(b.q), bf16(b.k_pool), bf16(b.v_pool), None, store[1:])
     torch.cuda.synchronize()
     assert_parity(f64(o), f64(lse), *run_oracle(b, packed_mask=packed))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_only_16_byte_aligned(d):
+    """O at an address that is 16- but not 32-byte aligned (the epilogue's
+    16-byte store path)."""
+    b = W.make_paged_batch(96, [70, 3, 130], [90, 40, 130], page_size=8, hq=8, hk=2, d=d)
+    attn = pka.BatchAttention()
+    attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, num_qo_heads=8, num_kv_heads=2,
+              head_dim=d, page_size=8, split_mode="off")
+    n = b.nnz_q * 8 * d
+    store = torch.zeros(n + 8, dtype=torch.bfloat16, device="cuda")
+    out = store[8:].view(b.nnz_q, 8, d)
+    assert out.data_ptr() % 32 == 16
+    o, lse = attn.run(bf16(b.q), bf16(b.k_pool), bf16(b.v_pool), i32(b.kv_indices), out=out)
+    torch.cuda.synchronize()
+    assert_parity(f64(o), f64(lse), *run_oracle(b))

@@ -115,7 +115,10 @@ typedef struct pka_plan_info {
   int32_t num_merge_tasks;   /* (row, qo head) pairs merged after a split     */
   int32_t num_partial_records;
   int32_t decode_chunk_tokens; /* keys per decode CTA (0: no split)            */
-  int32_t reserved[5];
+  int32_t num_decode_joins;  /* split (decode row, kv head) pairs that the     */
+                             /* decode kernel merges itself (their g qo heads  */
+                             /* are among num_merge_tasks)                     */
+  int32_t reserved[4];
 } pka_plan_info;
 
 typedef struct pka_plan_s* pka_plan_t;
@@ -208,6 +211,13 @@ pka_status pka_plan_wait(pka_plan_t plan);
  *   kv_indices_d are ignored.
  *   packed_mask_d: little-endian bit array, read only for PKA_MASK_CUSTOM.
  *   float_ws_d: at least info.float_ws_bytes (may be NULL when that is 0).
+ *   Split decode rows are merged inside the decode kernel: each piece counts
+ *   itself in a counter of the device plan image, and the last one merges.
+ *   The counters return to zero by the end of every run, so one plan serves
+ *   any number of runs; two runs of one plan must not overlap on the GPU
+ *   (they would share the counters and the float workspace).  After
+ *   PKA_ERR_DEVICE_TIMEOUT a counter may be left non-zero: call pka_plan
+ *   again (it rewrites the image) before the next run.
  *   Returns PKA_ERR_STALE_PLAN when *params differs from the planned one. */
 pka_status pka_run(pka_plan_t plan, const pka_params* params, const void* q, const void* k,
                    const void* v, int64_t page_stride, const int32_t* kv_indices_d,

@@ -19,7 +19,17 @@
 // P^T comes from the S^T fragments by an in-register 8x8 transpose
 // (movmatrix).  A CTA writes the final bf16 output and base-2 LSE of a
 // request, or, when the plan split the request, a normalised fp32 partial
-// state for the merge kernel.
+// state.  The pieces of a split request count themselves in a join counter
+// of the plan image, and the last one merges the pieces' states ("A worked
+// split-KV example") and writes O and the LSE, so no separate merge launch
+// follows the decode kernel.  A consumer warp that finds (from a read of the
+// counter during its last tile) that every other piece has finished merges
+// them with its own state in registers.  Otherwise it writes its partial
+// state.  For a CTA's last item it then counts the piece in itself, and
+// merges from the workspace if that completes the count (each warp its own
+// kv head, in parallel).  Earlier split pieces go to the CTA's join warp,
+// which makes their states visible GPU-wide and counts them in while the
+// consumers go on with the next item.
 //
 // HND pages of 8 or a multiple of 16 slots take a second staging layout: each
 // kv head's 16 keys arrive by TMA as [16 rows x 128 B] blocks with the
@@ -39,6 +49,7 @@ namespace {
 
 constexpr int TS = kDecodeTileTokens;  // keys per stage = one m16 MMA block
 constexpr int kMaxStages = 4;
+constexpr int kJoinRing = 4;  // split pieces in flight between the consumers and the join warp
 constexpr int kStageBudget = 200 * 1024;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
@@ -104,6 +115,100 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
+}
+
+// n-way merge of the pieces of one split (request, kv head) for its G qo
+// heads, all read from the float workspace ("Deep Dive - FlashInfer", "Core
+// mechanism" and "A worked split-KV example"): with b_k the pieces' base-2
+// statistics, m = max b_k and s = sum 2^(b_k - m), o = sum (2^(b_k - m) / s)
+// o_k and lse = m + log2 s; pieces with b_k = -inf carry no weight, and if
+// all are empty o = 0 and lse = -inf.  Every lane owns D / 32 dims of every
+// head and folds the (piece, head) pairs in one at a time (a running max with
+// rescaling), so all lanes hold the same statistics and nothing is exchanged.
+// The states come from other SMs and are read through L2 (.cg), 16 pairs
+// per round, all loads of a round issued before any is used.
+template <int D, int G>
+__device__ __noinline__ void join_merge_g(const AttnArgs& a, const PkaDecodeJoin j, int row,
+                                          int head0, int lane) {
+  constexpr int PER = D / 32;
+  constexpr int CH = G == 8 ? 8 : 12;  // pairs per round; a multiple of G (pair q is head q % G)
+  const int pairs = j.nslots * G;
+  float m[G], s[G], acc[G][PER];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    s[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[h][e] = 0.f;
+  }
+  for (int p0 = 0; p0 < pairs; p0 += CH) {
+    float b[CH], x[CH][PER];
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+      const int p = p0 + q;
+      const bool ok = p < pairs;
+      const int64_t rec = j.rec_first + (int64_t)(p / G) * j.rec_stride + q % G;
+      b[q] = ok ? __ldcg(a.part_lse + rec) : -INFINITY;
+      const float* src = a.part_o + (ok ? rec : 0) * D + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 v = ok ? __ldcg(reinterpret_cast<const float4*>(src))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[q][0] = v.x;
+        x[q][1] = v.y;
+        x[q][2] = v.z;
+        x[q][3] = v.w;
+      } else {
+        const float2 v = ok ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+        x[q][0] = v.x;
+        x[q][1] = v.y;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < CH; ++q) {
+      const int h = q % G;
+      if (b[q] == -INFINITY) continue;
+      if (b[q] > m[h]) {
+        const float sc = exp2f(m[h] - b[q]);  // 0 while m is -inf
+        s[h] = s[h] * sc + 1.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[h][e] = acc[h][e] * sc + x[q][e];
+        m[h] = b[q];
+      } else {
+        const float wq = exp2f(b[q] - m[h]);
+        s[h] += wq;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[h][e] += wq * x[q][e];
+      }
+    }
+  }
+  const int Hq = a.num_qo_heads;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const bool any = s[h] > 0.f;
+    const float inv = any ? 1.f / s[h] : 0.f;
+    const int64_t oi = (int64_t)row * Hq + head0 + h;
+    uint16_t* dst = a.o + oi * D + lane * PER;
+    if constexpr (PER == 4) {
+      uint2 pk;
+      pk.x = float2_to_bf16x2(acc[h][0] * inv, acc[h][1] * inv);
+      pk.y = float2_to_bf16x2(acc[h][2] * inv, acc[h][3] * inv);
+      *reinterpret_cast<uint2*>(dst) = pk;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = float2_to_bf16x2(acc[h][0] * inv, acc[h][1] * inv);
+    }
+    if (lane == 0 && a.lse) a.lse[oi] = any ? m[h] + log2f(s[h]) : -INFINITY;
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void join_merge(const AttnArgs& a, const PkaDecodeJoin& j, int row,
+                                           int head0, int G, int lane) {
+  switch (G) {
+    case 1: join_merge_g<D, 1>(a, j, row, head0, lane); break;
+    case 2: join_merge_g<D, 2>(a, j, row, head0, lane); break;
+    case 4: join_merge_g<D, 4>(a, j, row, head0, lane); break;
+    default: join_merge_g<D, 8>(a, j, row, head0, lane); break;
+  }
 }
 
 // Issue the bulk copies of keys [a0, a0 + n) of item w (K and V) into a stage.
@@ -191,13 +296,19 @@ __device__ __forceinline__ void issue_tile_swizzled(const AttnArgs& a, const Dec
   }
 }
 
+// Warps: consumers 0 .. hpc - 1 (one per kv head), producer hpc, join warp hpc + 1.
 template <int D>
-__global__ void __launch_bounds__(288, 1)
+__global__ void __launch_bounds__(320, 1)
     decode_kernel(const __grid_constant__ DecodeMaps maps, const AttnArgs a, const int stages) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ volatile int abort_flag;
+  // Handoff of split pieces to the join warp: per slot, one arrival per
+  // consumer warp (jfull) and a release by the join warp (jempty); jneed[s][hl]
+  // says whether kv head hl's partial state still has to be counted in.
+  __shared__ uint64_t jfull[kJoinRing], jempty[kJoinRing];
+  __shared__ int jneed[kJoinRing][8];
   constexpr int KS = D / 16;  // k-steps of the QK^T product
   constexpr int MT = D / 16;  // 16-dim blocks of the P V product
   const int hpc = a.heads_per_cta;
@@ -222,6 +333,10 @@ __global__ void __launch_bounds__(288, 1)
     for (int s = 0; s < stages; ++s) {
       mbar_init(bars.full(s), 33);  // expect_tx by lane 0 + the 32 producer lanes
       mbar_init(bars.empty(s), n_cons);
+    }
+    for (int s = 0; s < kJoinRing; ++s) {
+      mbar_init(smem_u32(&jfull[s]), n_cons);
+      mbar_init(smem_u32(&jempty[s]), 1);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -262,7 +377,48 @@ __global__ void __launch_bounds__(288, 1)
       if (!mbar_wait(bars.full(k % stages), (k / stages) & 1)) record_timeout(a.err, &abort_flag);
     return;
   }
-  if (warp > n_cons) return;
+  if (warp == n_cons + 1) {
+    // ---------------- join warp ----------------
+    // Takes the split pieces before the CTA's last item, in the consumers'
+    // order.  For every kv head whose consumer wrote a partial state: fence
+    // (the consumers' stores reach it through the CTA-scope barrier, the fence
+    // makes them visible GPU-wide), count the piece in, and if that completes
+    // the count merge all pieces (rare: such a piece is normally the first
+    // item of its CTA, and its unit's other pieces end later).
+    uint32_t jc = 0;
+    for (int ii = i0; ii < i1 - 1 && !abort_flag; ++ii) {
+      const PkaWorkItem w = a.items[ii];
+      if (w.join < 0 || !a.joins) continue;
+      const int s = jc % kJoinRing;
+      if (!mbar_wait(smem_u32(&jfull[s]), (jc / kJoinRing) & 1)) {
+        record_timeout(a.err, &abort_flag);
+        break;
+      }
+      const int need = lane < n_cons ? jneed[s][lane] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&jempty[s]));
+      ++jc;
+      if (!__ballot_sync(0xffffffffu, need)) continue;
+      __threadfence();
+      int last = 0;
+      if (need) {
+        PkaDecodeJoin* jp = a.joins + w.join + lane;
+        last = atomicAdd(&jp->arrived, 1) == jp->nslots - 1;
+      }
+      uint32_t lm = __ballot_sync(0xffffffffu, last);
+      if (lm) __threadfence();
+      while (lm) {
+        const int hq = __ffs(lm) - 1;
+        lm &= lm - 1;
+        PkaDecodeJoin* jq = a.joins + w.join + hq;
+        join_merge<D>(a, *jq, w.q_row0, (w.kv_head0 + hq) * G, G, lane);
+        __syncwarp();
+        if (lane == 0) jq->arrived = 0;  // every piece has arrived: re-arm for the next run
+      }
+    }
+    return;
+  }
+  if (warp > n_cons + 1) return;
 
   // ---------------- consumer warps: warp hl serves kv head kv_head0 + hl ----------------
   const int hl = warp;
@@ -281,10 +437,15 @@ __global__ void __launch_bounds__(288, 1)
   };
   const uint32_t sK0 = smem_u32(sK), sV0 = smem_u32(sV);
   const float sc = a.scale_log2;
-  uint32_t it = 0;
+  uint32_t it = 0, jc = 0;
   for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
     const PkaWorkItem w = a.items[ii];
     const int head_base = (w.kv_head0 + hl) * G;  // first qo head of this kv head
+    // split piece: the join's fixed fields now, the counter during the last tile
+    PkaDecodeJoin* jp = (w.join >= 0 && a.joins) ? a.joins + w.join + hl : nullptr;
+    PkaDecodeJoin jv{};
+    if (jp) jv = *jp;
+    int hint = -1;
     // Q^T fragments (k = dims, n = heads): head grp, dims 16ks + 2qd (+1, +8, +9)
     uint32_t qf[KS][2];
     {
@@ -307,6 +468,8 @@ __global__ void __launch_bounds__(288, 1)
 
     for (int a0 = w.t0; a0 < w.t1; a0 += TS, ++it) {
       const int s = it % stages;
+      if (jp && a0 + TS >= w.t1 && lane == 0)
+        hint = *reinterpret_cast<volatile int32_t*>(&jp->arrived);
       if (!mbar_wait(bars.full(s), (it / stages) & 1)) {
         record_timeout(a.err, &abort_flag);
         break;
@@ -392,34 +555,75 @@ __global__ void __launch_bounds__(288, 1)
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+    // Write O and the LSE, or this piece's partial state.  A split piece
+    // whose counter read (issued during the last tile) shows every other
+    // piece finished then merges all of them at once.
+    const bool merge_now = jp && __shfl_sync(0xffffffffu, hint, 0) == jv.nslots - 1;
+    {
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int h = 2 * qd + hh;  // head of this lane's accumulator columns
-      if (h >= G) continue;
-      const float l = hh ? l1 : l0, m = hh ? m1 : m0;
-      const bool any = l > 0.f;
-      const float inv = any ? 1.f / l : 0.f;
-      const float lse_v = any ? m + log2f(l) : -INFINITY;
-      const int head = head_base + h;
-      if (w.out_rec < 0) {
-        uint16_t* orow = a.o + ((int64_t)w.q_row0 * Hq + head) * D;
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 2 * qd + hh;  // head of this lane's accumulator columns
+        if (h >= G) continue;
+        const float l = hh ? l1 : l0, m = hh ? m1 : m0;
+        const bool any = l > 0.f;
+        const float inv = any ? 1.f / l : 0.f;
+        const float lse_v = any ? m + log2f(l) : -INFINITY;
+        const int head = head_base + h;
+        if (w.out_rec < 0) {
+          uint16_t* orow = a.o + ((int64_t)w.q_row0 * Hq + head) * D;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t pk = float2_to_bf16x2(acc[mt][hh] * inv, acc[mt][2 + hh] * inv);
-          orow[16 * mt + grp] = (uint16_t)(pk & 0xffffu);
-          orow[16 * mt + grp + 8] = (uint16_t)(pk >> 16);
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t pk = float2_to_bf16x2(acc[mt][hh] * inv, acc[mt][2 + hh] * inv);
+            orow[16 * mt + grp] = (uint16_t)(pk & 0xffffu);
+            orow[16 * mt + grp + 8] = (uint16_t)(pk >> 16);
+          }
+          if (grp == 0 && a.lse) a.lse[(int64_t)w.q_row0 * Hq + head] = lse_v;
+        } else {
+          const int rec = w.out_rec + (head - w.kv_head0 * G);
+          float* prow = a.part_o + (int64_t)rec * D;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            prow[16 * mt + grp] = acc[mt][hh] * inv;
+            prow[16 * mt + grp + 8] = acc[mt][2 + hh] * inv;
+          }
+          if (grp == 0) a.part_lse[rec] = lse_v;
         }
-        if (grp == 0 && a.lse) a.lse[(int64_t)w.q_row0 * Hq + head] = lse_v;
-      } else {
-        const int rec = w.out_rec + (head - w.kv_head0 * G);
-        float* prow = a.part_o + (int64_t)rec * D;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          prow[16 * mt + grp] = acc[mt][hh] * inv;
-          prow[16 * mt + grp + 8] = acc[mt][2 + hh] * inv;
-        }
-        if (grp == 0) a.part_lse[rec] = lse_v;
       }
+    }
+    bool do_merge = merge_now;
+    if (jp && !merge_now && ii + 1 == i1) {
+      // the CTA's last item: count the piece in here; the fence makes this
+      // lane's partial state visible GPU-wide before the arrival
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(&jp->arrived, 1) == jv.nslots - 1;
+      do_merge = __shfl_sync(0xffffffffu, last, 0) != 0;
+    }
+    if (do_merge) {
+      // this warp's own state was just written (the warp barrier orders it
+      // for the other lanes); the fence, after the counter read or the
+      // arrival, orders the other pieces' states before the reads
+      __syncwarp();
+      __threadfence();
+      join_merge<D>(a, jv, w.q_row0, head_base, G, lane);
+      __syncwarp();
+      if (lane == 0) jp->arrived = 0;  // every piece is done: re-arm for the next run
+    }
+    if (jp && ii + 1 < i1) {
+      // hand the piece to the join warp (kv head hl still to count in or not)
+      __syncwarp();
+      if (lane == 0) {
+        const int js = jc % kJoinRing;
+        if (jc >= (uint32_t)kJoinRing &&
+            !mbar_wait(smem_u32(&jempty[js]), ((jc / kJoinRing) - 1) & 1)) {
+          record_timeout(a.err, &abort_flag);
+        } else {
+          jneed[js][hl] = merge_now ? 0 : 1;
+          mbar_arrive(smem_u32(&jfull[js]));
+        }
+      }
+      ++jc;
     }
   }
 }
@@ -471,7 +675,7 @@ cudaError_t launch_t(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D><<<num_ctas, 32 * (hpc + 1), smem, stream>>>(maps, a, stages);
+  decode_kernel<D><<<num_ctas, 32 * (hpc + 2), smem, stream>>>(maps, a, stages);
   return cudaGetLastError();
 }
 

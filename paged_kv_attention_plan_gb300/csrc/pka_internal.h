@@ -12,6 +12,7 @@ namespace pka {
 struct AttnArgs {
   const int32_t* cta_ptr;     // [num_ctas + 1] item ranges per CTA
   const PkaWorkItem* items;
+  PkaDecodeJoin* joins;       // decode: joins of split units (plan image), or null
   const uint16_t* q;          // bf16 bits [nnz_q, Hq, D]
   const uint16_t* k;          // bf16 bits, pool or ragged tensor
   const uint16_t* v;

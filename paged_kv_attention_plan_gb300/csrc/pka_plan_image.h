@@ -3,7 +3,8 @@
 // host planner and the kernels (both are the product path).
 //
 // image := header | decode_cta_ptr | decode_items | prefill_cta_ptr |
-//          prefill_items | merge_tasks | merge_slots   (offsets in int32 units)
+//          prefill_items | merge_tasks | merge_slots | decode_joins
+//          (offsets in int32 units)
 #pragma once
 #include <stdint.h>
 
@@ -26,6 +27,9 @@ struct PkaImageHeader {
   int32_t decode_heads_per_cta;  // kv heads one decode CTA covers
   int32_t graph_mode;            // 1: fixed layout sized by the graph capacities
   int32_t off_merge_slots;       // int32[num_partial_records] record lists, 0 if none
+  int32_t num_decode_joins;      // split decode (request, kv head) pairs merged in the decode kernel
+  int32_t off_decode_joins;      // PkaDecodeJoin[num_decode_joins], 0 if none
+  int32_t reserved[14];
 };
 
 // One unit of attention work: a block of kv heads (decode) or one kv head
@@ -46,7 +50,7 @@ struct PkaWorkItem {
   int32_t mask_lo;     // mask_indptr[req] (bit offset), low/high words
   int32_t mask_hi;
   int32_t flags;
-  int32_t reserved;
+  int32_t join;        // decode piece of a split: first PkaDecodeJoin of its unit, else -1
 };
 
 // One (query row, qo head) whose partial states are merged after a split.
@@ -61,9 +65,22 @@ struct PkaMergeTask {
   int32_t reserved[3];
 };
 
+// One kv head of a split decode unit (request, block of kv heads).  Every
+// piece of the unit writes its partial states, then counts itself in
+// `arrived`; the piece that brings the count to nslots merges the states of
+// the kv head's g qo heads (records rec_first + k * rec_stride + h, k <
+// nslots, h < g) and sets `arrived` back to 0 for the next run.
+struct PkaDecodeJoin {
+  int32_t arrived;     // pieces finished so far in the current run (0 between runs)
+  int32_t rec_first;   // record of qo head 0 of this kv head in piece 0
+  int32_t nslots;      // pieces of the unit (>= 2)
+  int32_t rec_stride;  // records between consecutive pieces
+};
+
 // Item flags
 #define PKA_ITEM_ALL_VISIBLE 1  // every key of the range is visible (cascade levels above the last)
 
-static_assert(sizeof(PkaImageHeader) == 64, "header size");
+static_assert(sizeof(PkaImageHeader) == 128, "header size");
+static_assert(sizeof(PkaDecodeJoin) == 16, "join size");
 static_assert(sizeof(PkaWorkItem) == 64, "work item size");
 static_assert(sizeof(PkaMergeTask) == 32, "merge task size");

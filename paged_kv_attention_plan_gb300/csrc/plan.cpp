@@ -82,7 +82,7 @@ bool graph_mode(const pka_params* p) { return p->graph_max_batch > 0; }
 // a CTA.  Tensor-core rows are not split in graph mode: one item per
 // (request, kv head, query tile) and sum_r ceil(Q_r / tq) <= ceil(R / tq) + B.
 struct GraphCaps {
-  int64_t dec_items = 0, pre_items = 0, merges = 0, records = 0;
+  int64_t dec_items = 0, pre_items = 0, merges = 0, records = 0, joins = 0;
 };
 
 GraphCaps graph_caps(const pka_params* p, int num_sms) {
@@ -94,7 +94,9 @@ GraphCaps graph_caps(const pka_params* p, int num_sms) {
   c.dec_items = B * (p->num_kv_heads / hpc) + 2 * (int64_t)num_sms + 2;
   c.pre_items = (int64_t)p->num_kv_heads * ((R + tq - 1) / tq + B);
   if (p->split_mode == PKA_SPLIT_AUTO) {
-    c.merges = B * p->num_qo_heads;
+    // split decode rows are merged inside the decode kernel (one join per
+    // split (request, kv head)); no merge tasks are left for the merge kernel
+    c.joins = B * p->num_kv_heads;
     c.records = c.dec_items * hpc * g;
   }
   return c;
@@ -176,6 +178,7 @@ PkaWorkItem make_item(const Batch& b, int r, int kv_head0, int n_kv_heads, int q
   it.mask_lo = (int32_t)(uint32_t)(b.mask_base[r] & 0xffffffffu);
   it.mask_hi = (int32_t)(b.mask_base[r] >> 32);
   it.flags = b.item_flags;
+  it.join = -1;
   return it;
 }
 
@@ -185,7 +188,9 @@ struct PlanLists {
   std::vector<int32_t> pre_cta_ptr{0};
   std::vector<PkaWorkItem> pre_items;
   std::vector<PkaMergeTask> merges;
+  std::vector<PkaDecodeJoin> joins;  // split decode units, merged in the decode kernel
   int32_t records = 0;
+  int32_t joined_pairs = 0;  // (row, qo head) pairs the decode kernel merges
   int32_t decode_chunk = 0;
   // Cascade: every piece writes partial records and each (row, head) merges
   // the records of all levels, listed in merge_slots.
@@ -198,14 +203,32 @@ struct PlanLists {
 // Give the pieces of one split unit their partial records and merge tasks.
 // `pieces` index into `items`; each piece writes q_count * heads records laid
 // out [token][qo head]; the heads are heads_total qo heads starting at head0.
+// With join_kv_heads > 0 (decode pieces outside a cascade) the unit gets one
+// PkaDecodeJoin per kv head instead of merge tasks: the decode kernel merges
+// the pieces itself, the last piece to finish doing the work.
 void assign_records(PlanLists* L, std::vector<PkaWorkItem>& items,
                     const std::vector<int>& pieces, int q_row0, int q_count, int head0,
-                    int heads_total) {
+                    int heads_total, int join_kv_heads = 0) {
   if (pieces.size() < 2 && !L->cascade) return;
   int per = q_count * heads_total;
   int base = L->records;
   for (size_t k = 0; k < pieces.size(); ++k) items[pieces[k]].out_rec = base + (int)k * per;
   L->records += (int)pieces.size() * per;
+  if (join_kv_heads > 0 && !L->cascade) {
+    const int g = heads_total / join_kv_heads;
+    const int j0 = (int)L->joins.size();
+    for (int hl = 0; hl < join_kv_heads; ++hl) {
+      PkaDecodeJoin j{};
+      j.arrived = 0;
+      j.rec_first = base + hl * g;
+      j.nslots = (int)pieces.size();
+      j.rec_stride = per;
+      L->joins.push_back(j);
+    }
+    for (int k : pieces) items[k].join = j0;
+    L->joined_pairs += q_count * heads_total;
+    return;
+  }
   if (L->cascade) {
     for (size_t k = 0; k < pieces.size(); ++k)
       for (int i = 0; i < q_count; ++i)
@@ -244,6 +267,50 @@ void build_slot_merges(PlanLists* L, int32_t nnz, int32_t heads) {
     t.nslots = start[k + 1] - start[k];
     t.rec_stride = 0;  // list mode
     L->merges.push_back(t);
+  }
+}
+
+// Order the items inside each decode CTA so that few split units have more
+// than one piece finishing at the end of the kernel.  The last of a unit's
+// pieces to finish merges them all: when it runs last in its CTA while
+// another piece of the unit also runs last in its own CTA, both finish
+// together, neither sees the other done in advance, and the merge takes the
+// slow path (fence, count, then the merge) right at the end.  A piece that
+// fills a whole CTA always ends last; among the other split pieces, those of
+// a CTA that also holds whole units go first, and a CTA with just two split
+// pieces runs last the one whose unit has no piece ending last yet (walking
+// the CTAs in order).
+void order_split_pieces(PlanLists* L) {
+  auto& items = L->dec_items;
+  const auto& ptr = L->dec_cta_ptr;
+  if (L->joins.empty()) return;
+  std::vector<int> ends(L->joins.size(), 0);  // pieces ending last, by the unit's first join
+  const int ctas = (int)ptr.size() - 1;
+  for (int c = 0; c < ctas; ++c)
+    if (ptr[c + 1] - ptr[c] == 1 && items[ptr[c]].join >= 0) ++ends[items[ptr[c]].join];
+  for (int c = 0; c < ctas; ++c) {
+    const int b = ptr[c], e = ptr[c + 1];
+    if (e - b < 2) continue;
+    std::vector<PkaWorkItem> split, whole;
+    for (int i = b; i < e; ++i) (items[i].join >= 0 ? split : whole).push_back(items[i]);
+    if (split.empty()) continue;
+    if (!whole.empty()) {
+      int i = b;
+      for (const auto& it : split) items[i++] = it;
+      for (const auto& it : whole) items[i++] = it;
+      continue;
+    }
+    if (split.size() != 2) continue;
+    // split[0] continues a unit from the previous CTA, split[1] goes on in the
+    // next: run split[0] last unless its unit already has a piece ending last
+    const int u = split[0].join, v = split[1].join;
+    if (ends[u] == 0) {
+      items[b] = split[1];
+      items[b + 1] = split[0];
+      ++ends[u];
+    } else {
+      ++ends[v];
+    }
   }
 }
 
@@ -293,7 +360,7 @@ void plan_decode(const pka_params* p, const std::vector<Batch>& lv, int num_sms,
         L->dec_cta_ptr.push_back((int)items.size());
         t = t1;
       } while (t < u.K);
-      assign_records(L, items, pieces, lv[u.l].q_row0[u.r], 1, u.hg * hpc * g, hpc * g);
+      assign_records(L, items, pieces, lv[u.l].q_row0[u.r], 1, u.hg * hpc * g, hpc * g, hpc);
     }
     return;
   }
@@ -322,9 +389,10 @@ void plan_decode(const pka_params* p, const std::vector<Batch>& lv, int num_sms,
         load = 0;
       }
     } while (t < u.K);
-    assign_records(L, items, pieces, lv[u.l].q_row0[u.r], 1, u.hg * hpc * g, hpc * g);
+    assign_records(L, items, pieces, lv[u.l].q_row0[u.r], 1, u.hg * hpc * g, hpc * g, hpc);
   }
   if (L->dec_cta_ptr.back() != (int)items.size()) L->dec_cta_ptr.push_back((int)items.size());
+  order_split_pieces(L);
 }
 
 // Rows of requests with qo_len >= 2 go to the tensor-core kernel: units are
@@ -486,7 +554,7 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
     fold_ctas(L.pre_cta_ptr, L.pre_items, num_sms);
     if ((int64_t)L.dec_items.size() > caps.dec_items ||
         (int64_t)L.pre_items.size() > caps.pre_items || (int64_t)L.merges.size() > caps.merges ||
-        L.records > caps.records) {
+        L.records > caps.records || (int64_t)L.joins.size() > caps.joins) {
       pka::set_last_error("plan outgrew the graph-mode image capacities");
       return PKA_ERR_WORKSPACE;
     }
@@ -496,6 +564,7 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   const int64_t n_dec = graph ? caps.dec_items : (int64_t)L.dec_items.size();
   const int64_t n_pre = graph ? caps.pre_items : (int64_t)L.pre_items.size();
   const int64_t n_merge = graph ? caps.merges : (int64_t)L.merges.size();
+  const int64_t n_join = graph ? caps.joins : (int64_t)L.joins.size();
   const int64_t layout_records = graph ? caps.records : L.records;
 
   PkaImageHeader h{};
@@ -506,6 +575,7 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   h.num_prefill_items = (int)L.pre_items.size();
   h.num_merge_tasks = (int)L.merges.size();
   h.num_partial_records = L.records;
+  h.num_decode_joins = (int)L.joins.size();
   h.decode_heads_per_cta =
       pka::decode_heads_per_cta(p->num_kv_heads, p->num_qo_heads / p->num_kv_heads);
   h.graph_mode = graph ? 1 : 0;
@@ -523,6 +593,9 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   w = align_words(w + n_merge * kMergeWords);
   h.off_merge_slots = L.merge_slots.empty() ? 0 : (int)w;
   w = align_words(w + L.merge_slots.size());
+  constexpr size_t kJoinWords = sizeof(PkaDecodeJoin) / 4;
+  h.off_decode_joins = n_join > 0 ? (int)w : 0;
+  w = align_words(w + n_join * kJoinWords);
   if (w > (size_t)INT32_MAX || layout_records > INT32_MAX / 256) {
     pka::set_last_error("plan image or partial records exceed 2^31");
     return PKA_ERR_UNSUPPORTED;
@@ -542,7 +615,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   info.num_decode_items = h.num_decode_items;
   info.num_prefill_ctas = h.num_prefill_ctas;
   info.num_prefill_items = h.num_prefill_items;
-  info.num_merge_tasks = h.num_merge_tasks;
+  info.num_merge_tasks = h.num_merge_tasks + L.joined_pairs;
+  info.num_decode_joins = h.num_decode_joins;
   info.num_partial_records = L.records;
   info.decode_chunk_tokens = L.decode_chunk;
   plan->info = info;
@@ -563,6 +637,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
                       h.off_prefill_items + L.pre_items.size() * kItemWords - h.off_prefill_cta_ptr});
     if (!L.merges.empty())
       ranges.push_back({(size_t)h.off_merge_tasks, L.merges.size() * kMergeWords});
+    if (!L.joins.empty())
+      ranges.push_back({(size_t)h.off_decode_joins, L.joins.size() * kJoinWords});
   } else {
     ranges.push_back({0, w});
   }
@@ -579,6 +655,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
     std::memcpy(img + h.off_merge_tasks, L.merges.data(), L.merges.size() * sizeof(PkaMergeTask));
   if (!L.merge_slots.empty())
     std::memcpy(img + h.off_merge_slots, L.merge_slots.data(), L.merge_slots.size() * 4);
+  if (!L.joins.empty())
+    std::memcpy(img + h.off_decode_joins, L.joins.data(), L.joins.size() * sizeof(PkaDecodeJoin));
 
   plan->params = *p;
   plan->hdr = h;
@@ -759,6 +837,9 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
   if (graph || h.num_decode_items > 0) {
     a.cta_ptr = plan->int_ws_d + h.off_decode_cta_ptr;
     a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_decode_items);
+    a.joins = h.off_decode_joins
+                  ? reinterpret_cast<PkaDecodeJoin*>(plan->int_ws_d + h.off_decode_joins)
+                  : nullptr;
     cudaError_t e = pka::launch_decode(a, h.num_decode_ctas, p->head_dim, g, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }

@@ -4,10 +4,12 @@ import numpy as np
 HEADER = ["magic", "total_words", "num_decode_ctas", "num_decode_items", "num_prefill_ctas",
           "num_prefill_items", "num_merge_tasks", "num_partial_records", "off_decode_cta_ptr",
           "off_decode_items", "off_prefill_cta_ptr", "off_prefill_items", "off_merge_tasks",
-          "decode_heads_per_cta", "graph_mode", "off_merge_slots"]
+          "decode_heads_per_cta", "graph_mode", "off_merge_slots", "num_decode_joins",
+          "off_decode_joins"]
 ITEM = ["req", "kv_head0", "n_kv_heads", "q_row0", "q_local0", "q_count", "qo_len", "kv_len",
-        "kv_base", "t0", "t1", "out_rec", "mask_lo", "mask_hi", "flags", "reserved"]
+        "kv_base", "t0", "t1", "out_rec", "mask_lo", "mask_hi", "flags", "join"]
 MERGE = ["out_row", "head", "rec_first", "nslots", "rec_stride"]
+JOIN = ["arrived", "rec_first", "nslots", "rec_stride"]
 
 
 def parse(buf: np.ndarray):
@@ -23,6 +25,11 @@ def parse(buf: np.ndarray):
     merges = [dict(zip(MERGE, map(int, w[h["off_merge_tasks"] + 8 * i:
                                           h["off_merge_tasks"] + 8 * i + 5])))
               for i in range(h["num_merge_tasks"])]
+    joins = []
+    if h["off_decode_joins"]:
+        o = h["off_decode_joins"]
+        joins = [dict(zip(JOIN, map(int, w[o + 4 * i: o + 4 * (i + 1)])))
+                 for i in range(h["num_decode_joins"])]
     slots = []
     if h["off_merge_slots"]:
         o = h["off_merge_slots"]
@@ -31,4 +38,4 @@ def parse(buf: np.ndarray):
             "decode_items": items(h["off_decode_items"], h["num_decode_items"]),
             "prefill_cta_ptr": [int(x) for x in pre_ptr],
             "prefill_items": items(h["off_prefill_items"], h["num_prefill_items"]),
-            "merges": merges}
+            "merges": merges, "joins": joins}

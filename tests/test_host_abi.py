@@ -169,7 +169,26 @@ def check_coverage(plan, b, hq, hk, causal, info, allow_empty_ctas=False):
             assert rec not in merged
             merged.add(rec)
         assert m["nslots"] >= 2
+    # split decode units: merged in the decode kernel through their joins
+    joins = plan["joins"]
+    for j in joins:
+        assert j["arrived"] == 0 and j["nslots"] >= 2
+        for k in range(j["nslots"]):
+            for h in range(g):
+                rec = j["rec_first"] + k * j["rec_stride"] + h
+                assert rec not in merged
+                merged.add(rec)
+    for it in plan["decode_items"]:
+        assert (it["join"] >= 0) == (it["out_rec"] >= 0)
+        if it["join"] >= 0:
+            for hl in range(hpc):
+                j = joins[it["join"] + hl]
+                k, r = divmod(it["out_rec"] + hl * g - j["rec_first"], j["rec_stride"])
+                assert r == 0 and 0 <= k < j["nslots"]
+    for it in plan["prefill_items"]:
+        assert it["join"] == -1
     assert merged == recs
+    assert info.num_decode_joins == len(joins)
     assert info.float_ws_bytes >= info.num_partial_records * (b.head_dim + 1) * 4
 
 

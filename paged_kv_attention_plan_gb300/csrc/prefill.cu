@@ -23,6 +23,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "pka_internal.h"
@@ -48,11 +49,15 @@ struct Maps {
   CUtensorMap q;     // 3-D {D, Hq, nnz_q}, box {64, g, 128/g}
   CUtensorMap kv_k;  // paged: 4-D, box = one whole page; ragged: 3-D, box 128 rows
   CUtensorMap kv_v;
+  CUtensorMap row_k;  // paged: the pool as 2-D rows of D elements, box {64, 1} (row gathers)
+  CUtensorMap row_v;
 };
 
 struct PrefillParams {
   AttnArgs a;
   int group;
+  int gather;              // 1: rows outside whole-page boxes come by TMA gather4
+  int64_t rows_per_page;   // page_stride / D: rows of the 2-D view per page
 };
 
 struct Bars {
@@ -132,10 +137,14 @@ __device__ __forceinline__ uint32_t kv_tile_tma_bytes(const PrefillParams& pp,
 // Issue the loads of one 128-key tile of K (or V) for kv head w.kv_head0:
 // rows [kb, vend) of the window; rows past vend keep older finite data and
 // are masked.  Lanes share the pages and rows of the window.
+// Returns whether this lane issued cp.async copies (generic-proxy writes the
+// caller has to wait for and fence before it arrives).
 template <int D>
-__device__ __forceinline__ void load_kv_tile(const PrefillParams& pp, const CUtensorMap* map,
-                                             const uint16_t* pool, const PkaWorkItem& w, int kb,
-                                             uint32_t dst, uint32_t bar, int lane) {
+__device__ __forceinline__ bool load_kv_tile(const PrefillParams& pp, const CUtensorMap* map,
+                                             const CUtensorMap& maps_row_k,
+                                             const CUtensorMap& maps_row_v, const uint16_t* pool,
+                                             const PkaWorkItem& w, int kb, uint32_t dst,
+                                             uint32_t bar, int lane) {
   constexpr int NB = D / 64;
   const AttnArgs& a = pp.a;
   if (a.kv_ragged) {
@@ -143,7 +152,7 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& pp, const CUte
 #pragma unroll
       for (int c = 0; c < NB; ++c)
         tc::tma_load_3d(dst + c * BLK, map, c * 64, w.kv_head0, w.kv_base + kb, bar);
-    return;
+    return false;
   }
   const int P = a.page_size;
   const int Hk = a.num_kv_heads;
@@ -160,23 +169,65 @@ __device__ __forceinline__ void load_kv_tile(const PrefillParams& pp, const CUte
         tc::tma_load_4d(d + c * BLK, map, c * 64, 0, w.kv_head0, page, bar);
     }
   }
-  // gathered rows: 16-byte chunks, swizzled by hand (chunk ^ (row & 7))
+  // Rows outside whole-page boxes.  With the 2-D row maps: one TMA gather4
+  // per four rows and 64-column block (each lane one group, its own bytes
+  // added to the barrier's count); a short last group repeats its last row
+  // (rows past the window hold finite data and are masked).  Without them, or
+  // for a group whose row index exceeds the 2-D map, 16-byte cp.async chunks
+  // swizzled by hand (chunk ^ (row & 7)).
   constexpr int CH = D / 8;  // 16-byte chunks per row
-  const int gathered = t.head_rows + (t.nrows - t.tail_start);
-  for (int x = lane; x < gathered * CH; x += 32) {
-    const int q = x / CH, ch = x - q * CH;
-    const int r = q < t.head_rows ? q : t.tail_start + (q - t.head_rows);
+  bool copied = false;
+  auto row_addr = [&](int r, int64_t& off, int64_t& row) {
     const int j = kb + r;
     const int pi = j / P;
     const int page = a.kv_indices[w.kv_base + pi];
     const int slot = j - pi * P;
-    const int64_t off = (int64_t)page * a.page_stride +
-                        (nhd ? ((int64_t)slot * Hk + w.kv_head0) * D
-                             : ((int64_t)w.kv_head0 * P + slot) * D) +
-                        ch * 8;
-    const uint32_t d = dst + (ch / 8) * BLK + r * 128 + (((ch % 8) ^ (r & 7)) * 16);
-    cp_async16(d, pool + off);
+    const int64_t in_page = nhd ? (int64_t)slot * Hk + w.kv_head0 : (int64_t)w.kv_head0 * P + slot;
+    off = (int64_t)page * a.page_stride + in_page * D;
+    row = (int64_t)page * pp.rows_per_page + in_page;
+  };
+  if (pp.gather) {
+    const int gh = (t.head_rows + 3) / 4, gt = (t.nrows - t.tail_start + 3) / 4;
+    const CUtensorMap* rmap = pool == a.k ? &maps_row_k : &maps_row_v;
+    for (int gi = lane; gi < gh + gt; gi += 32) {
+      const int r0 = gi < gh ? 4 * gi : t.tail_start + 4 * (gi - gh);
+      const int rend = gi < gh ? t.head_rows : t.nrows;
+      int64_t off[4], row[4];
+      bool fits = true;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        row_addr(min(r0 + q, rend - 1), off[q], row[q]);
+        fits = fits && row[q] < ((int64_t)1 << 31);
+      }
+      if (fits) {
+        tc::mbar_expect_tx(bar, (uint32_t)(4 * 128 * NB));
+#pragma unroll
+        for (int c = 0; c < NB; ++c)
+          tc::tma_gather4(dst + c * BLK + r0 * 128, rmap, c * 64, (int)row[0], (int)row[1],
+                          (int)row[2], (int)row[3], bar);
+      } else {
+        for (int q = 0; q < 4 && r0 + q < rend; ++q)
+          for (int ch = 0; ch < CH; ++ch) {
+            const int r = r0 + q;
+            cp_async16(dst + (ch / 8) * BLK + r * 128 + (((ch % 8) ^ (r & 7)) * 16),
+                       pool + off[q] + ch * 8);
+          }
+        copied = true;
+      }
+    }
+    return copied;
   }
+  const int gathered = t.head_rows + (t.nrows - t.tail_start);
+  for (int x = lane; x < gathered * CH; x += 32) {
+    const int q = x / CH, ch = x - q * CH;
+    const int r = q < t.head_rows ? q : t.tail_start + (q - t.head_rows);
+    int64_t off, row;
+    row_addr(r, off, row);
+    const uint32_t d = dst + (ch / 8) * BLK + r * 128 + (((ch % 8) ^ (r & 7)) * 16);
+    cp_async16(d, pool + off + ch * 8);
+    copied = true;
+  }
+  return copied;
 }
 
 // 128 consecutive mask bits starting at bit `start` (little-endian bit order);
@@ -333,12 +384,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bytes = kv_tile_tma_bytes<D>(pp, w, kb);
         if (lane == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), bytes);
         __syncwarp();
-        load_kv_tile<D>(pp, map, pool, w, kb, smem_u32(ring + s * NB * BLK), smem_u32(&full[s]),
-                        lane);
-        // Gathered rows are generic-proxy writes: wait for this lane's copies,
-        // make them visible to the tensor cores, then arrive.
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        tc::fence_proxy_async_smem();
+        const bool copied =
+            load_kv_tile<D>(pp, map, maps.row_k, maps.row_v, pool, w, kb,
+                            smem_u32(ring + s * NB * BLK), smem_u32(&full[s]), lane);
+        // Rows copied with cp.async are generic-proxy writes: wait for this
+        // lane's copies and make them visible to the tensor cores before the
+        // arrival.  TMA rows complete on the barrier by themselves.
+        if (copied) {
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          tc::fence_proxy_async_smem();
+        }
         mbar_arrive(smem_u32(&full[s]));
       }
     }
@@ -690,12 +745,14 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
 }
 
 template <int D>
-cudaError_t launch_t(const PrefillParams& pp, int num_ctas, int nnz_q, int64_t total_kv,
+cudaError_t launch_t(PrefillParams pp, int num_ctas, int nnz_q, int64_t total_kv,
                      cudaStream_t stream) {
   const AttnArgs& a = pp.a;
+  int pp_gather = 0;
   const int G = pp.group;
   const uint64_t Hq = a.num_qo_heads, Hk = a.num_kv_heads;
   Maps maps;
+  std::memset(&maps, 0, sizeof(maps));
   {
     const uint64_t dims[3] = {(uint64_t)D, Hq, (uint64_t)(nnz_q > 0 ? nnz_q : 1)};
     const uint64_t str[2] = {(uint64_t)D * 2, Hq * D * 2};
@@ -727,6 +784,17 @@ cudaError_t launch_t(const PrefillParams& pp, int num_ctas, int nnz_q, int64_t t
     }
     if (!encode(&maps.kv_k, a.k, 4, dims, str, box) || !encode(&maps.kv_v, a.v, 4, dims, str, box))
       return cudaErrorInvalidValue;
+    // The pool as rows of D elements (one kv head of one slot), for gather4:
+    // row = page * (page_stride / D) + the slot's and head's row in the page.
+    if (a.page_stride % D == 0) {
+      const uint64_t rdims[2] = {(uint64_t)D, (uint64_t)1 << 31};
+      const uint64_t rstr[1] = {(uint64_t)D * 2};
+      const uint32_t rbox[2] = {64, 1};
+      if (!encode(&maps.row_k, a.k, 2, rdims, rstr, rbox) ||
+          !encode(&maps.row_v, a.v, 2, rdims, rstr, rbox))
+        return cudaErrorInvalidValue;
+      pp_gather = 1;
+    }
   }
   constexpr int NB = D / 64;
   // At least 120 KiB, so that one CTA (and its 512 TMEM columns) owns each SM.
@@ -735,6 +803,8 @@ cudaError_t launch_t(const PrefillParams& pp, int num_ctas, int nnz_q, int64_t t
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  pp.gather = pp_gather;
+  pp.rows_per_page = pp_gather ? a.page_stride / D : 0;
   prefill_kernel<D><<<num_ctas, kThreads, smem, stream>>>(maps, pp);
   return cudaGetLastError();
 }

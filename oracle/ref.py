@@ -25,6 +25,13 @@ pages it cites; nothing is blocked, fused or reordered:
 * "KV-Cache layouts", section "Multi-level cascade inference data layout"
   (per-level qo_indptr / kv_indptr / kv_indices / last_page_len over one
   pool): cascade_attention.
+* 8-bit K/V: the e4m3 format as its published definition states it (OCP
+  "8-bit floating point" specification: 1 sign bit, 4 exponent bits with
+  bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN), and the pages'
+  note that low-precision caches use the HND layout ("KV-Cache layouts",
+  "NHD/HND").  The pages give no scale contract; the reading taken is one
+  scale per K pool and one per V pool: a stored code c stands for
+  e4m3(c) * scale.
 
 Readings where the pages are silent (each is listed in the design notes):
 bit 1 of a custom mask keeps a key; the mask is applied after scaling; a row
@@ -53,6 +60,32 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns to float64 (exact: bf16 is the top half of fp32)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Decode e4m3 codes (uint8) to float64 by the format's definition.
+
+    sign s = bit 7, exponent e = bits 6..3 (bias 7), mantissa m = bits 2..0:
+    e = 0 is subnormal, (-1)^s * m/8 * 2^(1-7); otherwise (-1)^s * (1 + m/8) *
+    2^(e-7), except e = 15 with m = 7, which is NaN (the format has no
+    infinities, so e = 15 with m < 7 are the largest finite values)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    out = sign * mag
+    return np.where((e == 15) & (c & 7 == 7), np.nan, out)
+
+
+def kv_payload_to_f64(x, kv_dtype: str, scale: float) -> np.ndarray:
+    """K or V payload as float64 values: bf16 bit patterns, or e4m3 codes
+    times the pool's scale."""
+    if kv_dtype == "bf16":
+        return bf16_bits_to_f64(x)
+    if kv_dtype == "e4m3":
+        return e4m3_to_f64(x) * float(scale)
+    raise ValueError(kv_dtype)
 
 
 # ---------------------------------------------------------------------------
@@ -245,13 +278,16 @@ def visible_keys(mode, i, qo_len, kv_len, packed_mask=None, mask_start=0):
 def batch_attention(q_bits, k_pool_bits, v_pool_bits, *, qo_indptr, kv_indptr, kv_indices,
                     last_page_len, page_size, num_qo_heads, num_kv_heads, layout="NHD",
                     mask_mode="causal", packed_mask=None, sm_scale=None, kv_ragged=False,
-                    requests=None, kv_range=None, rows=None):
+                    requests=None, kv_range=None, rows=None, kv_dtype="bf16", k_scale=1.0,
+                    v_scale=1.0):
     """Reference output of one batch.
 
     Returns (o, lse2) as float64 arrays [nnz_q, Hq, D] and [nnz_q, Hq]; rows of
     requests not listed in ``requests`` stay NaN.  ``kv_range`` (t0, t1)
     restricts every request to logical keys t0 <= j < t1 (a split-KV chunk).
-    ``rows`` (a set of global query rows) computes only those rows."""
+    ``rows`` (a set of global query rows) computes only those rows.
+    ``kv_dtype`` "e4m3": the pools hold e4m3 codes standing for
+    e4m3(code) * k_scale (K) and e4m3(code) * v_scale (V)."""
     q = bf16_bits_to_f64(q_bits)
     head_dim = q.shape[-1]
     if num_qo_heads % num_kv_heads:
@@ -275,12 +311,12 @@ def batch_attention(q_bits, k_pool_bits, v_pool_bits, *, qo_indptr, kv_indptr, k
             raise ValueError("causal attention needs kv_len >= qo_len")
         if rows is not None and not any(int(qo_indptr[r]) + i in rows for i in range(qlen)):
             continue
-        kr = bf16_bits_to_f64(gather_request_kv(
+        kr = kv_payload_to_f64(gather_request_kv(
             k_pool_bits, layout=layout, page_size=page_size, kv_indptr=kv_indptr,
-            kv_indices=kv_indices, req=r, kv_len=klen, kv_ragged=kv_ragged))
-        vr = bf16_bits_to_f64(gather_request_kv(
+            kv_indices=kv_indices, req=r, kv_len=klen, kv_ragged=kv_ragged), kv_dtype, k_scale)
+        vr = kv_payload_to_f64(gather_request_kv(
             v_pool_bits, layout=layout, page_size=page_size, kv_indptr=kv_indptr,
-            kv_indices=kv_indices, req=r, kv_len=klen, kv_ragged=kv_ragged))
+            kv_indices=kv_indices, req=r, kv_len=klen, kv_ragged=kv_ragged), kv_dtype, v_scale)
         for i in range(qlen):
             row = int(qo_indptr[r]) + i
             if rows is not None and row not in rows:

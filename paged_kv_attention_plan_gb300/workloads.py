@@ -29,6 +29,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 BF16_NAN_BITS = np.uint16(0x7FC1)
+E4M3_NAN_CODE = np.uint8(0x7F)  # the e4m3 NaN (exponent and mantissa all ones)
 
 NHD = "NHD"
 HND = "HND"
@@ -81,6 +82,9 @@ class Batch:
     k_pool: np.ndarray | None = None
     v_pool: np.ndarray | None = None
     mask_bool: np.ndarray | None = None  # flattened uint8 0/1, custom mask only
+    kv_dtype: str = "bf16"  # "bf16" bit patterns, or "e4m3" codes (uint8 pools)
+    k_scale: float = 1.0  # e4m3 pools: a code c stands for e4m3(c) * scale
+    v_scale: float = 1.0
     k_new: np.ndarray | None = None  # appended rows [nnz_q, Hk, D] (bits)
     v_new: np.ndarray | None = None
     extra: dict = field(default_factory=dict)
@@ -125,24 +129,42 @@ def build_page_table(rng, kv_lens, page_size, pool_pages=None, page_ids=None):
     return kv_indptr, np.asarray(page_ids, dtype=np.int32), last, int(pool_pages)
 
 
-def fill_pool(rng, kv_lens, kv_indptr, kv_indices, page_size, pool_pages, hk, d, layout):
-    """Pool tensors with N(0,1) bf16 payload in used slots and NaN elsewhere."""
+def e4m3_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Random e4m3 codes of either sign with exponent field 3..8 and any
+    mantissa: magnitudes 1/16 .. 3.75, an N(0,1)-like spread that stays away
+    from the format's subnormals, its largest values and its NaN."""
+    sign = rng.integers(0, 2, size=shape).astype(np.uint8) << 7
+    exp = rng.integers(3, 9, size=shape).astype(np.uint8) << 3
+    man = rng.integers(0, 8, size=shape).astype(np.uint8)
+    return (sign | exp | man).astype(np.uint8)
+
+
+def fill_pool(rng, kv_lens, kv_indptr, kv_indices, page_size, pool_pages, hk, d, layout,
+              kv_dtype="bf16"):
+    """Pool tensors with payload in used slots and NaN elsewhere: N(0,1) bf16
+    bit patterns, or e4m3 codes (kv_dtype "e4m3")."""
     shape = (pool_pages, page_size, hk, d) if layout == NHD else (pool_pages, hk, page_size, d)
-    k = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
-    v = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
+    if kv_dtype == "e4m3":
+        k = np.full(shape, E4M3_NAN_CODE, dtype=np.uint8)
+        v = np.full(shape, E4M3_NAN_CODE, dtype=np.uint8)
+    else:
+        k = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
+        v = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
     fill_pages(rng, k, v, kv_lens, kv_indptr, kv_indices, page_size, layout)
     return k, v
 
 
 def fill_pages(rng, k, v, kv_lens, kv_indptr, kv_indices, page_size, layout):
-    """Write N(0,1) bf16 rows into the slots of each request's pages, in place."""
+    """Write random rows (N(0,1) bf16, or e4m3 codes for a uint8 pool) into
+    the slots of each request's pages, in place."""
+    draw = e4m3_codes if k.dtype == np.uint8 else normal_bf16_bits
     for r, n in enumerate(np.asarray(kv_lens)):
         n = int(n)
         if n == 0:
             continue
-        rows_k = normal_bf16_bits(rng, (n,) + k.shape[-2:] if layout == NHD else
-                                  (n, k.shape[1], k.shape[3]))
-        rows_v = normal_bf16_bits(rng, rows_k.shape)
+        rows_k = draw(rng, (n,) + k.shape[-2:] if layout == NHD else
+                      (n, k.shape[1], k.shape[3]))
+        rows_v = draw(rng, rows_k.shape)
         pages = kv_indices[kv_indptr[r]:kv_indptr[r + 1]]
         for j0 in range(0, n, page_size):
             pg = int(pages[j0 // page_size])
@@ -157,7 +179,8 @@ def fill_pages(rng, k, v, kv_lens, kv_indptr, kv_indices, page_size, layout):
 
 def make_paged_batch(seed, qo_lens, kv_lens, *, page_size, layout=NHD, hq=32, hk=8, d=128,
                      mask_mode="causal", pool_pages=None, page_ids=None, name="paged",
-                     is_decode=False, with_payload=True, append_new=False):
+                     is_decode=False, with_payload=True, append_new=False, kv_dtype="bf16",
+                     k_scale=1.0, v_scale=1.0):
     """Generic paged batch.  With ``append_new`` the last ``qo_len`` positions
     of every request are left as NaN in the pool and their rows are returned in
     ``k_new``/``v_new`` instead (they are what append_paged_kv_cache writes)."""
@@ -169,12 +192,13 @@ def make_paged_batch(seed, qo_lens, kv_lens, *, page_size, layout=NHD, hq=32, hk
     b = Batch(name=name, num_qo_heads=hq, num_kv_heads=hk, head_dim=d, page_size=page_size,
               layout=layout, mask_mode=mask_mode, qo_lens=qo_lens, kv_lens=kv_lens,
               qo_indptr=_prefix(qo_lens), kv_indptr=kv_indptr, kv_indices=kv_indices,
-              last_page_len=last, is_decode=is_decode)
+              last_page_len=last, is_decode=is_decode, kv_dtype=kv_dtype, k_scale=k_scale,
+              v_scale=v_scale)
     b.extra["pool_pages"] = pool
     if with_payload:
         b.q = normal_bf16_bits(rng, (b.nnz_q, hq, d))
         b.k_pool, b.v_pool = fill_pool(rng, kv_lens, kv_indptr, kv_indices, page_size, pool,
-                                       hk, d, layout)
+                                       hk, d, layout, kv_dtype)
         if append_new:
             b.k_new = np.empty((b.nnz_q, hk, d), dtype=np.uint16)
             b.v_new = np.empty((b.nnz_q, hk, d), dtype=np.uint16)
@@ -320,13 +344,15 @@ def worked_example(seed=1000, literal_pages=False, hq=4, hk=2, d=64):
 
 
 def batch_decode(seed=1001, n=64, kv_lo=512, kv_hi=4096, page_size=16, layout=NHD, hq=32,
-                 hk=8, d=128, with_payload=True):
-    """64 decode requests, kv_len ~ U[512, 4096], page size 16, 32/8 heads."""
+                 hk=8, d=128, with_payload=True, kv_dtype="bf16", k_scale=1.0, v_scale=1.0):
+    """64 decode requests, kv_len ~ U[512, 4096], page size 16, 32/8 heads
+    (K/V as bf16, or as e4m3 codes with per-pool scales)."""
     rng = np.random.default_rng(seed)
     kv = rng.integers(kv_lo, kv_hi, size=n, endpoint=True)
     return make_paged_batch(seed + 7, np.ones(n, np.int32), kv, page_size=page_size,
                             layout=layout, hq=hq, hk=hk, d=d, mask_mode="causal",
-                            name="batch_decode", is_decode=True, with_payload=with_payload)
+                            name="batch_decode", is_decode=True, with_payload=with_payload,
+                            kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale)
 
 
 def append_prefill(seed=1002, n=16, q_lo=128, q_hi=1024, prefix_hi=4096, page_size=16,

@@ -152,29 +152,32 @@ def time_steps(fn, steps, warmup, stream, l2_buf=None):
 # Workloads
 # ---------------------------------------------------------------------------
 
-def decode_setup(device):
+def decode_setup(device, kv_dtype="bf16"):
+    """Batch-decode workload; kv_dtype "e4m3" stores K/V as 8-bit codes (one
+    scale per pool), halving the K/V bytes per key."""
     import paged_kv_attention_plan_gb300 as pka
     from paged_kv_attention_plan_gb300 import workloads as W
-    from tests.gpu_util import bf16, i32
+    from tests.gpu_util import bf16, i32, kv_tensor
 
-    b = W.batch_decode(seed=1001)
-    d = dict(batch=b, q=bf16(b.q, device), k=bf16(b.k_pool, device), v=bf16(b.v_pool, device),
-             idx=i32(b.kv_indices, device))
+    b = W.batch_decode(seed=1001, kv_dtype=kv_dtype, k_scale=0.5, v_scale=2.0)
+    d = dict(batch=b, q=bf16(b.q, device), k=kv_tensor(b.k_pool, device),
+             v=kv_tensor(b.v_pool, device), idx=i32(b.kv_indices, device))
     attn = pka.BatchAttention(device=device)
-    info = attn.plan(None, b.kv_indptr, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
-                     head_dim=128, page_size=16, split_mode="auto")
+    kw = dict(num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16, split_mode="auto",
+              kv_dtype=kv_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
+    info = attn.plan(None, b.kv_indptr, b.last_page_len, **kw)
     d["attn"], d["info"] = attn, info
     t = []
     for _ in range(20):  # host time of one plan() (validation, planning, image, async copy)
         t0 = time.perf_counter()
-        attn.plan(None, b.kv_indptr, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
-                  head_dim=128, page_size=16, split_mode="auto")
+        attn.plan(None, b.kv_indptr, b.last_page_len, **kw)
         t.append(time.perf_counter() - t0)
     d["plan_us"] = statistics.median(t) * 1e6
     d["o"] = torch.empty_like(d["q"])
     d["lse"] = torch.empty(b.nnz_q, 32, dtype=torch.float32, device=device)
     kv_tokens = int(np.sum(b.kv_lens))
-    d["kv_bytes"] = kv_tokens * 8 * 128 * 2 * 2
+    d["kv_tokens"] = kv_tokens
+    d["kv_bytes"] = kv_tokens * 8 * 128 * (1 if kv_dtype == "e4m3" else 2) * 2
     d["bytes"] = d["kv_bytes"] + 2 * d["q"].numel() * 2 + d["lse"].numel() * 4
     # split decode rows are merged inside the decode kernel; the merge kernel
     # only runs for states it does not cover
@@ -457,8 +460,8 @@ def reference_arm(args, rank):
 
 def profile_one(name, device, stream, steps, warmup, pk):
     """Run one workload's steps only (used under ncu); prints its timings."""
-    if name == "decode":
-        d = decode_setup(device)
+    if name in ("decode", "decode_fp8"):
+        d = decode_setup(device, "e4m3" if name == "decode_fp8" else "bf16")
         ms = time_steps(lambda: decode_step(d), steps, warmup, stream)
         out = {"workload": "batch_decode", "ms": statistics.median(ms),
                "GB/s": d["bytes"] / (statistics.median(ms) * 1e-3) / 1e9}
@@ -491,8 +494,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "prefill", "ragged", "mixed1",
-                                                          "mixed16", "cascade"],
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "decode_fp8", "prefill",
+                                                          "ragged", "mixed1", "mixed16", "cascade"],
                     help="all (default) prints the benchmark line; a single workload only runs "
                          "that workload's kernels (for profiling) and prints its numbers")
     args = ap.parse_args()
@@ -551,6 +554,21 @@ def main():
             "algorithmic_bytes": d["bytes"],
             "kernel": "decode_kernel<128> (one run(); split states merged in-kernel)",
             "peak_source": pk["source"]}
+
+    # ---- the same decode batch over e4m3 K/V (half the bytes per key)
+    d8 = decode_setup(device, "e4m3")
+    f8_ms = statistics.median(time_steps(lambda: decode_step(d8), 200, 5, stream))
+    fp8_decode = {"workload": "batch_decode over e4m3 K/V (k_scale 0.5, v_scale 2): same requests "
+                              "and heads as the bf16 line",
+                  "ms_per_step": f8_ms, "GB/s": d8["bytes"] / (f8_ms * 1e-3) / 1e9,
+                  "kv_tokens_per_s": d8["kv_tokens"] / (f8_ms * 1e-3),
+                  "bf16_kv_tokens_per_s": d["kv_tokens"] / (step_ms * 1e-3),
+                  "roofline": {"bound": "hbm", "achieved": d8["bytes"] / (f8_ms * 1e-3) / 1e9,
+                               "peak": pk["hbm_gbs"], "unit": "GB/s",
+                               "frac": d8["bytes"] / (f8_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                               "kernel": "decode_kernel<128, e4m3>"}}
+    del d8
+    torch.cuda.empty_cache()
 
     # ---- append + prefill (tensor cores)
     pf = prefill_setup(device)
@@ -642,7 +660,8 @@ def main():
                        "kv_bytes_per_step": d["kv_bytes"], "bytes_per_step": d["bytes"],
                        "l2": "inputs (604 MB of K/V) larger than L2; no flush",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roof, "prefill": prefill, "ragged_custom_mask": ragged,
+            "roofline": roof, "fp8_kv_decode": fp8_decode, "prefill": prefill,
+            "ragged_custom_mask": ragged,
             "mixed_step": mixed, "cascade": cascade, "e2e": e2e,
             "gpu_launches": d["launches"] * args.steps,
             "clocks": clocks.summary(), "plan": d["info"].as_dict(),

@@ -70,6 +70,14 @@ typedef enum pka_mask_mode {
   PKA_MASK_CUSTOM = 2   /* bit mask_indptr[r] + i*K + j of the packed mask; */
                         /* 1 keeps the key, 0 drops it                       */
 } pka_mask_mode;
+/* K/V element type.  PKA_KV_FP8_E4M3: the pools hold 8-bit e4m3 codes (the
+ * OCP 8-bit float format: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits); code c of the K pool stands for e4m3(c) * k_scale, of the V pool for
+ * e4m3(c) * v_scale.  The pages tie low-precision caches to the HND layout
+ * ("KV-Cache layouts", "NHD/HND") but fix no scale contract: one scale per
+ * pool is the plainest reading.  Decode rows only (qo_len == 1), any layout
+ * and page size; page_stride (in elements = bytes) a multiple of 16. */
+typedef enum pka_kv_dtype { PKA_KV_BF16 = 0, PKA_KV_FP8_E4M3 = 1 } pka_kv_dtype;
 typedef enum pka_split_mode {
   PKA_SPLIT_OFF = 0,    /* one work item per (request, head block, q tile)   */
   PKA_SPLIT_AUTO = 1,   /* planner balances keys across CTAs, merges splits  */
@@ -97,6 +105,9 @@ typedef struct pka_params {
   int32_t graph_max_batch;     /* the most requests of any plan                */
   int32_t graph_max_qo_rows;   /* the most query rows; q and o hold this many   */
   int32_t graph_max_kv_tokens; /* ragged K/V only: the most K/V rows            */
+  int32_t kv_dtype;            /* pka_kv_dtype of the K/V pools                 */
+  float k_scale;               /* PKA_KV_FP8_E4M3: scale of K codes (<= 0: 1)    */
+  float v_scale;               /* PKA_KV_FP8_E4M3: scale of V codes (<= 0: 1)    */
   int32_t reserved[2];         /* must be zero                                  */
 } pka_params;
 
@@ -133,8 +144,9 @@ pka_status pka_version(int32_t* major, int32_t* minor);
  * qo_indptr_h may be NULL (decode: one row per request).  Host only; needs
  * no GPU.  Returns PKA_ERR_METADATA for: indptr[0] != 0, a decreasing
  * indptr, a request with no page, last_page_len outside 1..P, causal rows
- * with kv_len < qo_len; PKA_ERR_UNSUPPORTED for head_dim not in {64,128} or a
- * head ratio not in {1,2,4,8}; PKA_ERR_INVALID_ARG for bad enums or sizes. */
+ * with kv_len < qo_len; PKA_ERR_UNSUPPORTED for head_dim not in {64,128}, a
+ * head ratio not in {1,2,4,8}, or e4m3 K/V with rows of qo_len >= 2;
+ * PKA_ERR_INVALID_ARG for bad enums or sizes. */
 pka_status pka_validate(const pka_params* params, int32_t batch, const int32_t* qo_indptr_h,
                         const int32_t* kv_indptr_h, const int32_t* last_page_len_h);
 
@@ -231,7 +243,7 @@ pka_status pka_run(pka_plan_t plan, const pka_params* params, const void* q, con
  *   last_page_len_d) already counts them, so row t lands at logical position
  *   kv_len - n_append + t.  Uses params->num_kv_heads, head_dim, page_size and
  *   layout.  Device metadata is trusted (not validated); nnz_new must equal
- *   append_indptr_d[batch]. */
+ *   append_indptr_d[batch].  bf16 pools only (PKA_ERR_UNSUPPORTED for e4m3). */
 pka_status pka_append_paged_kv_cache(const pka_params* params, int32_t batch, const void* k_new,
                                      const void* v_new, const int32_t* append_indptr_d,
                                      int64_t nnz_new, const int32_t* kv_indptr_d,

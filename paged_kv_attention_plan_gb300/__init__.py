@@ -10,7 +10,8 @@ from __future__ import annotations
 import torch
 
 from . import _pka
-from ._pka import (PKA_HND, PKA_MASK_CAUSAL, PKA_MASK_CUSTOM, PKA_MASK_NONE, PKA_NHD,  # noqa
+from ._pka import (PKA_HND, PKA_KV_BF16, PKA_KV_FP8_E4M3, PKA_MASK_CAUSAL,  # noqa
+                   PKA_MASK_CUSTOM, PKA_MASK_NONE, PKA_NHD,
                    PKA_SPLIT_AUTO, PKA_SPLIT_FIXED, PKA_SPLIT_OFF, PkaError, make_params,
                    pka_append_paged_kv_cache, pka_get_device_error, pka_last_error, pka_merge_states,
                    pka_packbits, pka_plan, pka_plan_cascade, pka_plan_create, pka_plan_destroy,
@@ -44,10 +45,12 @@ class BatchAttention:
     def plan(self, qo_indptr, kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, head_dim,
              page_size=1, layout="NHD", mask_mode="causal", sm_scale=0.0, kv_ragged=False,
              split_mode="auto", fixed_split_pages=1, num_sms=0, graph_max_batch=0,
-             graph_max_qo_rows=0, graph_max_kv_tokens=0, stream=None):
+             graph_max_qo_rows=0, graph_max_kv_tokens=0, kv_dtype="bf16", k_scale=1.0,
+             v_scale=1.0, stream=None):
         params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, layout, mask_mode,
                              sm_scale, kv_ragged, split_mode, fixed_split_pages, num_sms,
-                             graph_max_batch, graph_max_qo_rows, graph_max_kv_tokens)
+                             graph_max_batch, graph_max_qo_rows, graph_max_kv_tokens, kv_dtype,
+                             k_scale, v_scale)
         return self._plan(params, "pka_plan", lambda: pka_plan(
             self.handle, params, qo_indptr, kv_indptr, last_page_len, self.int_ws, self.pinned,
             stream, check=False))

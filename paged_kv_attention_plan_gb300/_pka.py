@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "libpka.so")
 PKA_NHD, PKA_HND = 0, 1
 PKA_MASK_NONE, PKA_MASK_CAUSAL, PKA_MASK_CUSTOM = 0, 1, 2
 PKA_SPLIT_OFF, PKA_SPLIT_AUTO, PKA_SPLIT_FIXED = 0, 1, 2
+PKA_KV_BF16, PKA_KV_FP8_E4M3 = 0, 1
 
 STATUS = {0: "PKA_OK", 1: "PKA_ERR_INVALID_ARG", 2: "PKA_ERR_METADATA", 3: "PKA_ERR_UNSUPPORTED",
           4: "PKA_ERR_WORKSPACE", 5: "PKA_ERR_STALE_PLAN", 6: "PKA_ERR_CUDA",
@@ -39,7 +40,8 @@ class pka_params(ctypes.Structure):
                 ("split_mode", ctypes.c_int32), ("fixed_split_pages", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("graph_max_batch", ctypes.c_int32),
                 ("graph_max_qo_rows", ctypes.c_int32), ("graph_max_kv_tokens", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float), ("reserved", ctypes.c_int32 * 2)]
 
 
 class pka_plan_info(ctypes.Structure):
@@ -160,12 +162,15 @@ def _dev(t, name, dtype):
     return t.data_ptr()
 
 
-def _dev_pool(t, name):
-    """K/V pool: the last three dims contiguous; pages may be strided (5-D view)."""
+def _dev_pool(t, name, params=None):
+    """K/V pool: the last three dims contiguous; pages may be strided (5-D view).
+    bf16, or uint8 e4m3 codes when the params say so."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
-    if t.dtype != torch.bfloat16:
-        raise TypeError(f"{name} must be torch.bfloat16, got {t.dtype}")
+    want = (torch.uint8 if params is not None and params.kv_dtype == PKA_KV_FP8_E4M3
+            else torch.bfloat16)
+    if t.dtype != want:
+        raise TypeError(f"{name} must be {want}, got {t.dtype}")
     if t.dim() >= 3 and (t.stride(-1) != 1 or t.stride(-2) != t.shape[-1]
                          or t.stride(-3) != t.shape[-1] * t.shape[-2]):
         raise ValueError(f"{name}: the last three dims must be contiguous")
@@ -181,7 +186,8 @@ def _stream(stream) -> int | None:
 def make_params(num_qo_heads, num_kv_heads, head_dim, page_size=1, layout="NHD",
                 mask_mode="causal", sm_scale=0.0, kv_ragged=False, split_mode="auto",
                 fixed_split_pages=1, num_sms=0, graph_max_batch=0, graph_max_qo_rows=0,
-                graph_max_kv_tokens=0) -> pka_params:
+                graph_max_kv_tokens=0, kv_dtype="bf16", k_scale=1.0,
+                v_scale=1.0) -> pka_params:
     p = pka_params()
     p.num_qo_heads, p.num_kv_heads, p.head_dim = num_qo_heads, num_kv_heads, head_dim
     p.page_size = page_size
@@ -197,6 +203,9 @@ def make_params(num_qo_heads, num_kv_heads, head_dim, page_size=1, layout="NHD",
     p.graph_max_batch = graph_max_batch
     p.graph_max_qo_rows = graph_max_qo_rows
     p.graph_max_kv_tokens = graph_max_kv_tokens
+    p.kv_dtype = ({"bf16": PKA_KV_BF16, "e4m3": PKA_KV_FP8_E4M3}[kv_dtype]
+                  if isinstance(kv_dtype, str) else kv_dtype)
+    p.k_scale, p.v_scale = k_scale, v_scale
     return p
 
 
@@ -286,8 +295,8 @@ def pka_run(handle, params, q, k, v, page_stride, kv_indices, packed_mask, o, ls
             stream=None, check=True) -> int:
     bf16 = torch.bfloat16
     fws = float_ws.numel() * float_ws.element_size() if float_ws is not None else 0
-    s = lib().pka_run(handle, ctypes.byref(params), _dev(q, "q", bf16), _dev_pool(k, "k"),
-                      _dev_pool(v, "v"), int(page_stride),
+    s = lib().pka_run(handle, ctypes.byref(params), _dev(q, "q", bf16),
+                      _dev_pool(k, "k", params), _dev_pool(v, "v", params), int(page_stride),
                       _dev(kv_indices, "kv_indices", torch.int32),
                       _dev(packed_mask, "packed_mask", torch.uint8), _dev(o, "o", bf16),
                       _dev(lse, "lse", torch.float32), _ptr(float_ws), fws, _stream(stream))
@@ -302,7 +311,8 @@ def pka_run_static_scratch(handle, params, q, k, v, page_stride, kv_indices, pac
     (no workspace from the caller; see include/pka.h)."""
     bf16 = torch.bfloat16
     s = lib().pka_run_static_scratch(
-        handle, ctypes.byref(params), _dev(q, "q", bf16), _dev_pool(k, "k"), _dev_pool(v, "v"),
+        handle, ctypes.byref(params), _dev(q, "q", bf16), _dev_pool(k, "k", params),
+        _dev_pool(v, "v", params),
         int(page_stride), _dev(kv_indices, "kv_indices", torch.int32),
         _dev(packed_mask, "packed_mask", torch.uint8), _dev(o, "o", bf16),
         _dev(lse, "lse", torch.float32), _stream(stream))
@@ -318,7 +328,8 @@ def pka_append_paged_kv_cache(params, k_new, v_new, append_indptr, kv_indptr, kv
         ctypes.byref(params), append_indptr.numel() - 1, _dev(k_new, "k_new", bf16),
         _dev(v_new, "v_new", bf16), _dev(append_indptr, "append_indptr", i32), k_new.shape[0],
         _dev(kv_indptr, "kv_indptr", i32), _dev(kv_indices, "kv_indices", i32),
-        _dev(last_page_len, "last_page_len", i32), _dev_pool(k, "k"), _dev_pool(v, "v"),
+        _dev(last_page_len, "last_page_len", i32), _dev_pool(k, "k", params),
+        _dev_pool(v, "v", params),
         int(page_stride),
         _stream(stream))
     if check:

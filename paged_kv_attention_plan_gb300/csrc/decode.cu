@@ -31,6 +31,16 @@
 // which makes their states visible GPU-wide and counts them in while the
 // consumers go on with the next item.
 //
+// e4m3 K/V (8-bit codes with one scale per pool) stages half the bytes per
+// key.  K fragments come straight from shared memory: one 32-bit load holds
+// four consecutive dims of a key, converted to f16 pairs; the dims of each
+// 16-wide k-block are taken in the order 0-3 | 4-7 | ... instead of the MMA's
+// 0,1,8,9 | 2,3,10,11 | ..., and Q's fragments follow the same order, so the
+// dot products are unchanged.  Each warp converts its kv head's V rows to f16
+// in a scratch tile read with ldmatrix.trans.  These MMAs run in f16 (e4m3
+// values are exact in f16; Q rounds to f16 once, P is in [0, 1]).  K's scale
+// is folded into the softmax scale and V's scale into the output.
+//
 // HND pages of 8 or a multiple of 16 slots take a second staging layout: each
 // kv head's 16 keys arrive by TMA as [16 rows x 128 B] blocks with the
 // 128-byte swizzle (16-byte chunk c of row r stored at chunk c ^ (r & 7)),
@@ -49,6 +59,7 @@ namespace {
 
 constexpr int TS = kDecodeTileTokens;  // keys per stage = one m16 MMA block
 constexpr int kMaxStages = 4;
+constexpr int kMaxStagesF8 = 6;
 constexpr int kJoinRing = 4;  // split pieces in flight between the consumers and the join warp
 constexpr int kStageBudget = 200 * 1024;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
@@ -60,8 +71,13 @@ struct Bars {
   __device__ uint32_t empty(int s) const { return smem_u32(base + stages + s); }
 };
 
-// Bytes of one key row in a stage: the CTA's kv heads, plus 16 bytes of pad.
-__host__ __device__ constexpr int row_bytes(int hpc, int D) { return hpc * D * 2 + 16; }
+// Bytes of one key row in a stage: the CTA's kv heads, plus 16 bytes of pad
+// (ES bytes per element: 2 for bf16, 1 for e4m3).
+__host__ __device__ constexpr int row_bytes(int hpc, int D, int ES = 2) {
+  return hpc * D * ES + 16;
+}
+// e4m3 path: a warp's f16 V scratch, [16 keys][D + 8] halves (padded rows).
+__host__ __device__ constexpr int vs_row_bytes(int D) { return (D + 8) * 2; }
 
 // Swizzled staging: one [16 keys x 64 dims] block is 2 KiB.
 constexpr int SWZ_BLK = TS * 128;
@@ -109,6 +125,52 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The same product with f16 operands (e4m3 K/V).
+__device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 codes (low byte first) -> two f16 (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  uint32_t r;
+  asm("{\n .reg .b16 c;\n cvt.u16.u32 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;\n}"
+      : "=r"(r)
+      : "r"(codes));
+  return r;
+}
+
+// Round two floats to f16 and pack them (low = a).
+__device__ __forceinline__ uint32_t float2_to_f16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
@@ -211,14 +273,17 @@ __device__ __forceinline__ void join_merge(const AttnArgs& a, const PkaDecodeJoi
   }
 }
 
-// Issue the bulk copies of keys [a0, a0 + n) of item w (K and V) into a stage.
-template <int D>
+// Issue the bulk copies of keys [a0, a0 + n) of item w (K and V) into a stage
+// (ES bytes per element).
+template <int D, int ES>
 __device__ __forceinline__ void issue_tile_copies(const AttnArgs& a, const PkaWorkItem& w,
                                                   int a0, int n, int hpc, uint32_t dK,
                                                   uint32_t dV, uint32_t bar, int lane) {
   const int Hk = a.num_kv_heads;
   const int P = a.page_size;
-  const int RS = row_bytes(hpc, D);
+  const int RS = row_bytes(hpc, D, ES);
+  const uint8_t* kp = reinterpret_cast<const uint8_t*>(a.k);
+  const uint8_t* vp = reinterpret_cast<const uint8_t*>(a.v);
   const int64_t row = (int64_t)Hk * D;  // elements of one token across all kv heads
   const bool head_major = a.layout == PKA_HND && P > 1 && !a.kv_ragged;
   if (!head_major) {
@@ -235,9 +300,9 @@ __device__ __forceinline__ void issue_tile_copies(const AttnArgs& a, const PkaWo
     }
     off += (int64_t)w.kv_head0 * D;
     if (lane < 16)
-      bulk_g2s(dK + t * RS, a.k + off, (uint32_t)(hpc * D * 2), bar);
+      bulk_g2s(dK + t * RS, kp + off * ES, (uint32_t)(hpc * D * ES), bar);
     else
-      bulk_g2s(dV + t * RS, a.v + off, (uint32_t)(hpc * D * 2), bar);
+      bulk_g2s(dV + t * RS, vp + off * ES, (uint32_t)(hpc * D * ES), bar);
     return;
   }
   // HND page [Hk, P, D]: one copy per (key, kv head, K or V)
@@ -247,8 +312,8 @@ __device__ __forceinline__ void issue_tile_copies(const AttnArgs& a, const PkaWo
     const int page = a.kv_indices[w.kv_base + j / P];
     const int64_t off =
         (int64_t)page * a.page_stride + ((int64_t)(w.kv_head0 + h) * P + (j % P)) * D;
-    const uint32_t d = (kv ? dV : dK) + t * RS + h * D * 2;
-    bulk_g2s(d, (kv ? a.v : a.k) + off, (uint32_t)(D * 2), bar);
+    const uint32_t d = (kv ? dV : dK) + t * RS + h * D * ES;
+    bulk_g2s(d, (kv ? vp : kp) + off * ES, (uint32_t)(D * ES), bar);
   }
 }
 
@@ -297,7 +362,8 @@ __device__ __forceinline__ void issue_tile_swizzled(const AttnArgs& a, const Dec
 }
 
 // Warps: consumers 0 .. hpc - 1 (one per kv head), producer hpc, join warp hpc + 1.
-template <int D>
+// F8: the K/V pools hold e4m3 codes.
+template <int D, bool F8>
 __global__ void __launch_bounds__(320, 1)
     decode_kernel(const __grid_constant__ DecodeMaps maps, const AttnArgs a, const int stages) {
   extern __shared__ uint8_t smem_raw[];
@@ -315,12 +381,16 @@ __global__ void __launch_bounds__(320, 1)
   const int G = a.num_qo_heads / a.num_kv_heads;
   const int n_cons = hpc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool swz = use_swizzled(a.layout, a.page_size, a.kv_ragged);
-  const int RS = row_bytes(hpc, D);
+  constexpr int ES = F8 ? 1 : 2;  // bytes per K/V element
+  const bool swz = !F8 && use_swizzled(a.layout, a.page_size, a.kv_ragged);
+  const int RS = row_bytes(hpc, D, ES);
   const int stage_bytes = swz ? hpc * (D / 64) * SWZ_BLK : TS * RS;
   uint8_t* sK = smem;
   uint8_t* sV = smem + stages * stage_bytes;
-  const Bars bars{reinterpret_cast<uint64_t*>(smem + 2 * stages * stage_bytes), stages};
+  uint8_t* sVc = smem + 2 * stages * stage_bytes;  // e4m3: per-warp f16 V scratch
+  const int scratch_bytes = F8 ? hpc * TS * vs_row_bytes(D) : 0;
+  const Bars bars{reinterpret_cast<uint64_t*>(smem + 2 * stages * stage_bytes + scratch_bytes),
+                  stages};
 
   const int i0 = a.cta_ptr[blockIdx.x], i1 = a.cta_ptr[blockIdx.x + 1];
   if (i0 >= i1) return;  // an empty CTA of a fixed (graph mode) grid
@@ -356,7 +426,8 @@ __global__ void __launch_bounds__(320, 1)
         }
         const int n = min(TS, w.t1 - a0);
         const int tx_rows = swz ? swz_tma_rows(a.page_size, n) : n;
-        if (lane == 0) mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * tx_rows * hpc * D * 2));
+        if (lane == 0)
+          mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * tx_rows * hpc * D * ES));
         __syncwarp();
         if (swz) {
           issue_tile_swizzled<D>(a, maps, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
@@ -365,8 +436,8 @@ __global__ void __launch_bounds__(320, 1)
           asm volatile("cp.async.wait_all;" ::: "memory");
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         } else {
-          issue_tile_copies<D>(a, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
-                               smem_u32(sV + s * stage_bytes), bars.full(s), lane);
+          issue_tile_copies<D, ES>(a, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
+                                   smem_u32(sV + s * stage_bytes), bars.full(s), lane);
         }
         mbar_arrive(bars.full(s));
       }
@@ -446,7 +517,9 @@ __global__ void __launch_bounds__(320, 1)
     PkaDecodeJoin jv{};
     if (jp) jv = *jp;
     int hint = -1;
-    // Q^T fragments (k = dims, n = heads): head grp, dims 16ks + 2qd (+1, +8, +9)
+    // Q^T fragments (k = dims, n = heads): head grp, dims 16ks + 2qd (+1, +8, +9);
+    // e4m3 K/V: dims 16ks + 4qd (+1 | +2, +3) in f16 (the k order of the K
+    // fragments read from e4m3 rows)
     uint32_t qf[KS][2];
     {
       const bool real = grp < G;
@@ -454,8 +527,16 @@ __global__ void __launch_bounds__(320, 1)
           a.q + ((int64_t)w.q_row0 * Hq + head_base + (real ? grp : 0)) * D);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        qf[ks][0] = real ? qrow[8 * ks + qd] : 0u;
-        qf[ks][1] = real ? qrow[8 * ks + 4 + qd] : 0u;
+        if constexpr (F8) {
+          const uint2 q4 = real ? *reinterpret_cast<const uint2*>(qrow + 8 * ks + 2 * qd)
+                                : make_uint2(0u, 0u);
+          const float2 f0 = bf16x2_to_float2(q4.x), f1 = bf16x2_to_float2(q4.y);
+          qf[ks][0] = float2_to_f16x2(f0.x, f0.y);
+          qf[ks][1] = float2_to_f16x2(f1.x, f1.y);
+        } else {
+          qf[ks][0] = real ? qrow[8 * ks + qd] : 0u;
+          qf[ks][1] = real ? qrow[8 * ks + 4 + qd] : 0u;
+        }
       }
     }
     float acc[MT][4];
@@ -478,11 +559,27 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t kb = sK0 + s * stage_bytes, vb = sV0 + s * stage_bytes;
       // S^T = K . Q^T
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (F8) {
+        // keys grp and grp + 8, dims 16ks + 4qd .. + 3 of each: one word each
+        const uint32_t k0 = kb + (uint32_t)(grp * RS + hl * D + 4 * qd);
+        const uint32_t k1 = k0 + 8 * RS;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t af[4];
-        ldsm_x4(kb + (swz ? swz_addr(k_key, 2 * ks + (mi >> 1)) : k_lane + 32 * ks), af);
-        mma16816(sacc, af, qf[ks][0], qf[ks][1]);
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t w0 = ld_shared_u32(k0 + 16 * ks), w1 = ld_shared_u32(k1 + 16 * ks);
+          uint32_t af[4];
+          af[0] = e4m3x2_to_f16x2(w0 & 0xffffu);
+          af[1] = e4m3x2_to_f16x2(w1 & 0xffffu);
+          af[2] = e4m3x2_to_f16x2(w0 >> 16);
+          af[3] = e4m3x2_to_f16x2(w1 >> 16);
+          mma16816_f16(sacc, af, qf[ks][0], qf[ks][1]);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t af[4];
+          ldsm_x4(kb + (swz ? swz_addr(k_key, 2 * ks + (mi >> 1)) : k_lane + 32 * ks), af);
+          mma16816(sacc, af, qf[ks][0], qf[ks][1]);
+        }
       }
       // keys grp and grp + 8 of the tile; heads 2qd, 2qd + 1
       bool ok0 = grp < n, ok1 = grp + 8 < n;
@@ -535,14 +632,46 @@ __global__ void __launch_bounds__(320, 1)
       l0 += p00 + p10;
       l1 += p01 + p11;
       // P^T fragments: transpose the (key x head) 8x8 blocks to (head x key)
-      const uint32_t pb0 = transpose8x8(float2_to_bf16x2(p00, p01));
-      const uint32_t pb1 = transpose8x8(float2_to_bf16x2(p10, p11));
-      // O^T += V^T . P^T
+      if constexpr (F8) {
+        const uint32_t pb0 = transpose8x8(float2_to_f16x2(p00, p01));
+        const uint32_t pb1 = transpose8x8(float2_to_f16x2(p10, p11));
+        // V rows of this kv head, e4m3 -> f16, into the warp's scratch (two
+        // lanes per key, D / 2 codes each), then O^T += V^T . P^T from it
+        const uint32_t vs = smem_u32(sVc) + (uint32_t)(hl * TS * vs_row_bytes(D));
+        {
+          constexpr int PL = D / 2;  // codes per lane
+          const int key = lane >> 1, half = lane & 1;
+          const uint32_t src = vb + (uint32_t)(key * RS + hl * D + half * PL);
+          const uint32_t dst = vs + (uint32_t)(key * vs_row_bytes(D) + half * PL * 2);
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        uint32_t af[4];
-        ldsm_x4_t(vb + (swz ? swz_addr(v_key, 2 * mt + (mi & 1)) : v_lane + 32 * mt), af);
-        mma16816(acc[mt], af, pb0, pb1);
+          for (int x = 0; x < PL / 16; ++x) {
+            const uint4 c = ld_shared_v4(src + 16 * x);
+            st_shared_v4(dst + 32 * x,
+                         make_uint4(e4m3x2_to_f16x2(c.x & 0xffffu), e4m3x2_to_f16x2(c.x >> 16),
+                                    e4m3x2_to_f16x2(c.y & 0xffffu), e4m3x2_to_f16x2(c.y >> 16)));
+            st_shared_v4(dst + 32 * x + 16,
+                         make_uint4(e4m3x2_to_f16x2(c.z & 0xffffu), e4m3x2_to_f16x2(c.z >> 16),
+                                    e4m3x2_to_f16x2(c.w & 0xffffu), e4m3x2_to_f16x2(c.w >> 16)));
+          }
+        }
+        __syncwarp();
+        const uint32_t vl = vs + (uint32_t)((mr + 8 * (mi >> 1)) * vs_row_bytes(D) + 16 * (mi & 1));
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t af[4];
+          ldsm_x4_t(vl + 32 * mt, af);
+          mma16816_f16(acc[mt], af, pb0, pb1);
+        }
+      } else {
+        const uint32_t pb0 = transpose8x8(float2_to_bf16x2(p00, p01));
+        const uint32_t pb1 = transpose8x8(float2_to_bf16x2(p10, p11));
+        // O^T += V^T . P^T
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t af[4];
+          ldsm_x4_t(vb + (swz ? swz_addr(v_key, 2 * mt + (mi & 1)) : v_lane + 32 * mt), af);
+          mma16816(acc[mt], af, pb0, pb1);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.empty(s));
@@ -566,7 +695,7 @@ __global__ void __launch_bounds__(320, 1)
         if (h >= G) continue;
         const float l = hh ? l1 : l0, m = hh ? m1 : m0;
         const bool any = l > 0.f;
-        const float inv = any ? 1.f / l : 0.f;
+        const float inv = any ? a.v_scale / l : 0.f;  // V's scale (1 for bf16 K/V)
         const float lse_v = any ? m + log2f(l) : -INFINITY;
         const int head = head_base + h;
         if (w.out_rec < 0) {
@@ -658,24 +787,27 @@ bool encode_hnd(CUtensorMap* m, const void* base, const AttnArgs& a, int D) {
          CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_t(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   const int hpc = a.heads_per_cta;
-  const bool swz = use_swizzled(a.layout, a.page_size, a.kv_ragged);
+  const bool swz = !F8 && use_swizzled(a.layout, a.page_size, a.kv_ragged);
   DecodeMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   if (swz && (!encode_hnd(&maps.k, a.k, a, D) || !encode_hnd(&maps.v, a.v, a, D)))
     return cudaErrorInvalidValue;
-  const int stage_bytes = 2 * (swz ? hpc * (D / 64) * SWZ_BLK : TS * row_bytes(hpc, D));
-  int stages = kStageBudget / stage_bytes;
-  if (stages > kMaxStages) stages = kMaxStages;
+  const int stage_bytes =
+      2 * (swz ? hpc * (D / 64) * SWZ_BLK : TS * row_bytes(hpc, D, F8 ? 1 : 2));
+  const int scratch = F8 ? hpc * TS * vs_row_bytes(D) : 0;
+  int stages = (kStageBudget - scratch) / stage_bytes;
+  if (stages > (F8 ? kMaxStagesF8 : kMaxStages)) stages = F8 ? kMaxStagesF8 : kMaxStages;
   if (stages < 2) return cudaErrorInvalidConfiguration;
   // the swizzled blocks need 1024-byte alignment: pad the dynamic allocation
-  const size_t smem = 1024 + (size_t)stages * stage_bytes + 2 * stages * sizeof(uint64_t);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>,
+  const size_t smem =
+      1024 + (size_t)stages * stage_bytes + scratch + 2 * stages * sizeof(uint64_t);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D><<<num_ctas, 32 * (hpc + 2), smem, stream>>>(maps, a, stages);
+  decode_kernel<D, F8><<<num_ctas, 32 * (hpc + 2), smem, stream>>>(maps, a, stages);
   return cudaGetLastError();
 }
 
@@ -686,8 +818,11 @@ cudaError_t launch_decode(const AttnArgs& a0, int num_ctas, int head_dim, int gr
   AttnArgs a = a0;
   a.err = device_error_word();
   (void)group;
-  if (head_dim == 128) return launch_t<128>(a, num_ctas, stream);
-  return launch_t<64>(a, num_ctas, stream);
+  if (a.kv_fp8)
+    return head_dim == 128 ? launch_t<128, true>(a, num_ctas, stream)
+                           : launch_t<64, true>(a, num_ctas, stream);
+  return head_dim == 128 ? launch_t<128, false>(a, num_ctas, stream)
+                         : launch_t<64, false>(a, num_ctas, stream);
 }
 
 }  // namespace pka

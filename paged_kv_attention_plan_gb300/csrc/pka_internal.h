@@ -30,7 +30,9 @@ struct AttnArgs {
   int32_t kv_ragged;
   int32_t mask_mode;
   int32_t heads_per_cta;      // decode: kv heads a CTA covers
-  float scale_log2;           // sm_scale * log2(e)
+  float scale_log2;           // sm_scale * log2(e) (times the K scale for e4m3 K/V)
+  int32_t kv_fp8;             // 1: k and v hold e4m3 codes (decode kernel only)
+  float v_scale;              // e4m3 V: scale of the codes (1 otherwise)
   int32_t* err;               // device error word (bounded waits that gave up)
 };
 

@@ -61,8 +61,11 @@ bool params_ok(const pka_params* p) {
   if (p->split_mode == PKA_SPLIT_FIXED && p->fixed_split_pages < 1) return false;
   if (!p->kv_ragged && p->page_size < 1) return false;
   if (p->num_sms < 0) return false;
+  if (p->kv_dtype != PKA_KV_BF16 && p->kv_dtype != PKA_KV_FP8_E4M3) return false;
+  if (!std::isfinite(p->k_scale) || !std::isfinite(p->v_scale)) return false;
   return true;
 }
+
 
 pka_status check_supported(const pka_params* p) {
   if (p->num_qo_heads % p->num_kv_heads) return PKA_ERR_UNSUPPORTED;
@@ -157,6 +160,15 @@ pka_status derive(const pka_params* p, int32_t batch, const int32_t* qo, const i
     b->mask_base[r + 1] = b->mask_base[r] + qlen * klen;
   }
   b->nnz_q = (int32_t)rows;
+  return PKA_OK;
+}
+
+// e4m3 K/V is read by the decode kernel only: rows with qo_len >= 2 (the
+// tensor-core path) are refused.
+pka_status check_kv_dtype(const pka_params* p, const Batch& b) {
+  if (p->kv_dtype != PKA_KV_FP8_E4M3) return PKA_OK;
+  for (int32_t q : b.qo_len)
+    if (q >= 2) return PKA_ERR_UNSUPPORTED;
   return PKA_OK;
 }
 
@@ -710,7 +722,8 @@ pka_status pka_validate(const pka_params* p, int32_t batch, const int32_t* qo,
   pka_status s = check_supported(p);
   if (s != PKA_OK) return s;
   Batch b;
-  return derive(p, batch, qo, kv, last, &b, p->mask_mode);
+  s = derive(p, batch, qo, kv, last, &b, p->mask_mode);
+  return s != PKA_OK ? s : check_kv_dtype(p, b);
 }
 
 pka_status pka_plan_create(pka_plan_t* plan) {
@@ -738,6 +751,7 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* p, int32_t batch, const i
   if (s != PKA_OK) return s;
   std::vector<Batch> lv(1);
   s = derive(p, batch, qo, kv, last, &lv[0], p->mask_mode);
+  if (s == PKA_OK) s = check_kv_dtype(p, lv[0]);
   if (s != PKA_OK) return s;
   return plan_levels(plan, p, lv, batch, false, int_ws_d, int_ws_bytes, pinned_h, pinned_bytes,
                      stream);
@@ -753,7 +767,9 @@ pka_status pka_plan_cascade(pka_plan_t plan, const pka_params* p, int32_t num_le
   plan->info = pka_plan_info{};
   pka_status s = check_supported(p);
   if (s != PKA_OK) return s;
-  if (p->kv_ragged || p->mask_mode == PKA_MASK_CUSTOM || graph_mode(p)) return PKA_ERR_UNSUPPORTED;
+  if (p->kv_ragged || p->mask_mode == PKA_MASK_CUSTOM || graph_mode(p) ||
+      p->kv_dtype != PKA_KV_BF16)
+    return PKA_ERR_UNSUPPORTED;
   if (num_levels < 1 || num_levels > PKA_MAX_CASCADE_LEVELS || !num_nodes || !qo || !kv || !last)
     return PKA_ERR_INVALID_ARG;
   std::vector<Batch> lv(num_levels);
@@ -800,7 +816,9 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
   // 16-byte alignment of every row the kernels move with vector or bulk copies
   const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
-  if ((mis & 15) || (!p->kv_ragged && (page_stride & 7))) return PKA_ERR_INVALID_ARG;
+  const bool fp8 = p->kv_dtype == PKA_KV_FP8_E4M3;
+  // page stride in elements: 16 bytes for bf16 (8 elements) or e4m3 (16)
+  if ((mis & 15) || (!p->kv_ragged && (page_stride & (fp8 ? 15 : 7)))) return PKA_ERR_INVALID_ARG;
   if (p->mask_mode == PKA_MASK_CUSTOM && !mask) return PKA_ERR_INVALID_ARG;
   if (float_ws_bytes < plan->info.float_ws_bytes || (plan->info.float_ws_bytes && !float_ws))
     return PKA_ERR_WORKSPACE;
@@ -830,7 +848,11 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
   a.kv_ragged = p->kv_ragged;
   a.mask_mode = p->mask_mode;
   a.heads_per_cta = h.decode_heads_per_cta;
-  a.scale_log2 = scale * 1.4426950408889634f;
+  // e4m3 K/V: K's scale multiplies every score, V's scale the output
+  const float k_scale = fp8 && p->k_scale > 0.f ? p->k_scale : 1.f;
+  a.scale_log2 = scale * k_scale * 1.4426950408889634f;
+  a.kv_fp8 = fp8 ? 1 : 0;
+  a.v_scale = fp8 && p->v_scale > 0.f ? p->v_scale : 1.f;
 
   // Graph mode launches every kernel on its fixed grid, whatever this plan
   // holds, so that a captured run() serves every later plan.
@@ -877,6 +899,7 @@ pka_status pka_append_paged_kv_cache(const pka_params* p, int32_t batch, const v
                                      void* k, void* v, int64_t page_stride, void* stream) {
   if (!params_ok(p) || batch < 0 || nnz_new < 0) return PKA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return PKA_ERR_UNSUPPORTED;
+  if (p->kv_dtype != PKA_KV_BF16) return PKA_ERR_UNSUPPORTED;  // no quantizing append
   if (p->kv_ragged) return PKA_ERR_UNSUPPORTED;
   if (nnz_new == 0 || batch == 0) return PKA_OK;
   if (!k_new || !v_new || !append_indptr || !kv_indptr || !kv_indices || !last_page_len || !k ||

@@ -24,6 +24,13 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+def kv_tensor(pool: np.ndarray, device="cuda") -> torch.Tensor:
+    """A K/V pool on the device: bf16 from bit patterns, or uint8 e4m3 codes."""
+    if pool.dtype == np.uint8:
+        return torch.from_numpy(np.ascontiguousarray(pool)).to(device)
+    return bf16(pool, device)
+
+
 def i32(a, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
 
@@ -34,9 +41,10 @@ def run_gpu(b, split=("auto", 1), packed_mask=None, attn=None, with_lse=True):
     info = attn.plan(qo, b.kv_indptr, b.last_page_len, num_qo_heads=b.num_qo_heads,
                      num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
                      layout=b.layout, mask_mode=b.mask_mode, kv_ragged=b.kv_ragged,
-                     split_mode=split[0], fixed_split_pages=split[1])
+                     split_mode=split[0], fixed_split_pages=split[1], kv_dtype=b.kv_dtype,
+                     k_scale=b.k_scale, v_scale=b.v_scale)
     q = bf16(b.q)
-    k, v = bf16(b.k_pool), bf16(b.v_pool)
+    k, v = kv_tensor(b.k_pool), kv_tensor(b.v_pool)
     idx = i32(b.kv_indices)
     mask = None if packed_mask is None else torch.from_numpy(packed_mask).cuda()
     o, lse = attn.run(q, k, v, idx, mask, return_lse=with_lse)
@@ -51,7 +59,8 @@ def run_oracle(b, packed_mask=None, rows=None):
                                last_page_len=b.last_page_len, page_size=b.page_size,
                                num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
                                layout=b.layout, mask_mode=b.mask_mode, packed_mask=packed_mask,
-                               sm_scale=b.sm_scale or None, kv_ragged=b.kv_ragged, rows=rows)
+                               sm_scale=b.sm_scale or None, kv_ragged=b.kv_ragged, rows=rows,
+                               kv_dtype=b.kv_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
 
 
 def assert_parity(o, lse, o_ref, lse_ref, rows=None):

@@ -41,11 +41,19 @@
 // values are exact in f16; Q rounds to f16 once, P is in [0, 1]).  K's scale
 // is folded into the softmax scale and V's scale into the output.
 //
-// HND pages of 8 or a multiple of 16 slots take a second staging layout: each
-// kv head's 16 keys arrive by TMA as [16 rows x 128 B] blocks with the
-// 128-byte swizzle (16-byte chunk c of row r stored at chunk c ^ (r & 7)),
-// and the ldmatrix addresses follow the swizzle; rows of a partial page are
-// gathered with 16-byte cp.async into the same layout.
+// Pages of 8 or a multiple of 16 slots (not ragged K/V, and e4m3 only with
+// D = 128) take a boxed staging layout instead: per 16-key tile, one TMA box
+// per 128-byte column block (64 bf16 dims or 128 e4m3 dims) and per K/V
+// brings the keys of all the CTA's kv heads, with the 128-byte swizzle
+// (16-byte chunk c of row r stored at chunk c ^ (r & 7)); the fragment
+// addresses follow the swizzle.  A few large copies per tile replace one
+// copy per key row.  An HND box is [heads][slots]: a head's consecutive keys
+// are consecutive rows.  An NHD box is [slots][heads]; its head count is
+// rounded up to an odd number (the extra head lies past the pool's last head
+// and is zero-filled, or belongs to the next head block), so that a head's
+// 8 consecutive keys fall in 8 different swizzle phases.  A tile's last keys
+// may lie past the request's end inside its last page: their scores are
+// replaced by -inf and their V rows by zeros before the P V product.
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -61,7 +69,9 @@ constexpr int TS = kDecodeTileTokens;  // keys per stage = one m16 MMA block
 constexpr int kMaxStages = 4;
 constexpr int kMaxStagesF8 = 6;
 constexpr int kJoinRing = 4;  // split pieces in flight between the consumers and the join warp
-constexpr int kStageBudget = 200 * 1024;
+// Dynamic shared memory for stages (and the e4m3 V scratch): 227 KiB less
+// the 1 KiB alignment pad, the barriers and the static variables.
+constexpr int kStageBudget = 227 * 1024 - 2048;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 struct Bars {
@@ -79,19 +89,23 @@ __host__ __device__ constexpr int row_bytes(int hpc, int D, int ES = 2) {
 // e4m3 path: a warp's f16 V scratch, [16 keys][D + 8] halves (padded rows).
 __host__ __device__ constexpr int vs_row_bytes(int D) { return (D + 8) * 2; }
 
-// Swizzled staging: one [16 keys x 64 dims] block is 2 KiB.
-constexpr int SWZ_BLK = TS * 128;
-
 struct DecodeMaps {
-  CUtensorMap k;  // HND pool {D, P, Hk, pages}, box {64, min(P, 16), 1, 1}
+  // boxed staging: NHD pool {D, Hk, P, pages}, box {cols, odd heads, R, 1};
+  // HND pool {D, P, Hk, pages}, box {cols, R, heads, 1}; R = min(P, 16)
+  CUtensorMap k;
   CUtensorMap v;
 };
 
 // Tiles start at multiples of 16 keys inside a request (the planner cuts
-// there) or at page boundaries, so with P = 8 or P a multiple of 16 every
-// box of min(P, 16) rows stays inside one page.
-__host__ __device__ inline bool use_swizzled(int layout, int P, int ragged) {
-  return layout == PKA_HND && !ragged && (P == 8 || P % 16 == 0);
+// there), so with P = 8 or P a multiple of 16 every box of min(P, 16) slots
+// stays inside one page.
+__host__ __device__ inline bool use_boxes(int P, int ragged, int D, int ES) {
+  return !ragged && (P == 8 || P % 16 == 0) && D * ES >= 128;
+}
+
+// Heads per box: the CTA's heads; an NHD box rounds them up to an odd count.
+__host__ __device__ inline int box_heads(int layout, int hpc) {
+  return layout == PKA_NHD ? (hpc | 1) : hpc;
 }
 
 __device__ __forceinline__ void record_timeout(int32_t* err, volatile int* abort_flag) {
@@ -317,55 +331,46 @@ __device__ __forceinline__ void issue_tile_copies(const AttnArgs& a, const PkaWo
   }
 }
 
-// Swizzled staging of keys [a0, a0 + n) (a0 is a multiple of 16): whole
-// boxes of R = min(P, 16) rows by TMA, the rest gathered with cp.async.
-// Rows of a tile of n keys that arrive by TMA (for expect_tx).
-__device__ __forceinline__ int swz_tma_rows(int P, int n) {
-  const int R = P < TS ? P : TS;
-  return (n / R) * R;
-}
-
-template <int D>
-__device__ __forceinline__ void issue_tile_swizzled(const AttnArgs& a, const DecodeMaps& maps,
-                                                    const PkaWorkItem& w, int a0, int n, int hpc,
-                                                    uint32_t dK, uint32_t dV, uint32_t bar,
-                                                    int lane) {
-  constexpr int NB = D / 64;
+// Boxed staging of keys [a0, a0 + n) (a0 is a multiple of 16): boxes of
+// R = min(P, 16) slots that hold at least one key of the tile, for every
+// 128-byte column block, K and V.  Issued by one lane; returns the bytes.
+template <int D, int ES>
+__device__ __forceinline__ uint32_t issue_tile_boxes(const AttnArgs& a, const DecodeMaps& maps,
+                                                     const PkaWorkItem& w, int a0, int n, int hb,
+                                                     uint32_t dK, uint32_t dV, uint32_t bar) {
+  constexpr int CW = 128 / ES;          // columns of one block
+  constexpr int NBc = D / CW;           // blocks per row
   const int P = a.page_size;
   const int R = P < TS ? P : TS;
-  const int full_rows = (n / R) * R;
-  // TMA: box i covers tile rows [i R, (i + 1) R) of one kv head and one 64-dim block
-  const int nbox = full_rows / R;
-  for (int x = lane; x < nbox * hpc * NB * 2; x += 32) {
-    const int kv = x & 1, c = (x >> 1) % NB, h = ((x >> 1) / NB) % hpc, i = (x >> 1) / NB / hpc;
-    const int j = a0 + i * R;
+  const uint32_t blk = (uint32_t)(TS * hb * 128);   // one block of a stage
+  const uint32_t box = (uint32_t)(R * hb * 128);    // one box
+  const int nbox = (n + R - 1) / R;
+  const bool nhd = a.layout == PKA_NHD;
+  for (int b = 0; b < nbox; ++b) {
+    const int j = a0 + b * R;
     const int page = a.kv_indices[w.kv_base + j / P];
-    const uint32_t dst = (kv ? dV : dK) + (h * NB + c) * SWZ_BLK + i * R * 128;
-    tc::tma_load_4d(dst, kv ? &maps.v : &maps.k, c * 64, j % P, w.kv_head0 + h, page, bar);
+    const int slot = j % P;
+#pragma unroll
+    for (int c = 0; c < NBc; ++c) {
+      const uint32_t off = c * blk + b * box;
+      if (nhd) {
+        tc::tma_load_4d(dK + off, &maps.k, c * CW, w.kv_head0, slot, page, bar);
+        tc::tma_load_4d(dV + off, &maps.v, c * CW, w.kv_head0, slot, page, bar);
+      } else {
+        tc::tma_load_4d(dK + off, &maps.k, c * CW, slot, w.kv_head0, page, bar);
+        tc::tma_load_4d(dV + off, &maps.v, c * CW, slot, w.kv_head0, page, bar);
+      }
+    }
   }
-  // cp.async: rows [full_rows, n), 16-byte chunks, swizzled by hand
-  constexpr int CH = D / 8;
-  const int rest = n - full_rows;
-  for (int x = lane; x < rest * hpc * CH * 2; x += 32) {
-    const int kv = x & 1, ch = (x >> 1) % CH, h = ((x >> 1) / CH) % hpc;
-    const int r = full_rows + (x >> 1) / CH / hpc;
-    const int j = a0 + r;
-    const int page = a.kv_indices[w.kv_base + j / P];
-    const int64_t off = (int64_t)page * a.page_stride +
-                        ((int64_t)(w.kv_head0 + h) * P + (j % P)) * D + ch * 8;
-    const uint32_t dst = (kv ? dV : dK) + (h * NB + ch / 8) * SWZ_BLK + r * 128 +
-                         (((ch % 8) ^ (r & 7)) * 16);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-                 "l"((kv ? a.v : a.k) + off)
-                 : "memory");
-  }
+  return (uint32_t)nbox * NBc * 2 * box;
 }
 
 // Warps: consumers 0 .. hpc - 1 (one per kv head), producer hpc, join warp hpc + 1.
 // F8: the K/V pools hold e4m3 codes.
 template <int D, bool F8>
 __global__ void __launch_bounds__(320, 1)
-    decode_kernel(const __grid_constant__ DecodeMaps maps, const AttnArgs a, const int stages) {
+    decode_kernel(const __grid_constant__ DecodeMaps maps, const AttnArgs a, const int stages,
+                  const int hb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -382,9 +387,11 @@ __global__ void __launch_bounds__(320, 1)
   const int n_cons = hpc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int ES = F8 ? 1 : 2;  // bytes per K/V element
-  const bool swz = !F8 && use_swizzled(a.layout, a.page_size, a.kv_ragged);
+  // hb > 0: boxed staging (hb heads per box row group, D * ES / 128 blocks of
+  // [16 keys x hb heads] 128-byte rows); hb == 0: one padded row per key
+  const bool boxed = hb > 0;
   const int RS = row_bytes(hpc, D, ES);
-  const int stage_bytes = swz ? hpc * (D / 64) * SWZ_BLK : TS * RS;
+  const int stage_bytes = boxed ? (D * ES / 128) * TS * hb * 128 : TS * RS;
   uint8_t* sK = smem;
   uint8_t* sV = smem + stages * stage_bytes;
   uint8_t* sVc = smem + 2 * stages * stage_bytes;  // e4m3: per-warp f16 V scratch
@@ -425,17 +432,18 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         const int n = min(TS, w.t1 - a0);
-        const int tx_rows = swz ? swz_tma_rows(a.page_size, n) : n;
-        if (lane == 0)
-          mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * tx_rows * hpc * D * ES));
-        __syncwarp();
-        if (swz) {
-          issue_tile_swizzled<D>(a, maps, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
-                                 smem_u32(sV + s * stage_bytes), bars.full(s), lane);
-          // gathered rows are generic-proxy writes: land, fence, then arrive
-          asm volatile("cp.async.wait_all;" ::: "memory");
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (boxed) {
+          if (lane == 0) {
+            const int R = a.page_size < TS ? a.page_size : TS;
+            mbar_arrive_expect_tx(bars.full(s), (uint32_t)(((n + R - 1) / R) * (D * ES / 128) *
+                                                           2 * R * hb * 128));
+            issue_tile_boxes<D, ES>(a, maps, w, a0, n, hb, smem_u32(sK + s * stage_bytes),
+                                    smem_u32(sV + s * stage_bytes), bars.full(s));
+          }
+          __syncwarp();
         } else {
+          if (lane == 0) mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * n * hpc * D * ES));
+          __syncwarp();
           issue_tile_copies<D, ES>(a, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
                                    smem_u32(sV + s * stage_bytes), bars.full(s), lane);
         }
@@ -500,12 +508,19 @@ __global__ void __launch_bounds__(320, 1)
   const int mi = lane >> 3, mr = lane & 7;
   const uint32_t k_lane = (uint32_t)((mr + 8 * (mi & 1)) * RS + hl * D * 2 + 16 * (mi >> 1));
   const uint32_t v_lane = (uint32_t)((mr + 8 * (mi >> 1)) * RS + hl * D * 2 + 16 * (mi & 1));
-  // swizzled staging: chunk c (16 bytes) of key row r of kv head hl
-  const uint32_t hb = (uint32_t)(hl * (D / 64) * SWZ_BLK);
-  const int k_key = mr + 8 * (mi & 1), v_key = mr + 8 * (mi >> 1);
-  auto swz_addr = [&](int key, int c) -> uint32_t {
-    return hb + (uint32_t)((c >> 3) * SWZ_BLK + key * 128 + (((c & 7) ^ (key & 7)) << 4));
+  // boxed staging: row of key t of kv head hl in a block, and the address of
+  // 16-byte chunk c of a row (blocks of 8 chunks, 128-byte swizzle)
+  const int R = a.page_size < TS ? a.page_size : TS;
+  const bool nhd = a.layout == PKA_NHD;
+  const uint32_t blk = (uint32_t)(TS * hb * 128);
+  auto box_row = [&](int t) -> int {
+    return nhd ? (t / R) * R * hb + (t % R) * hb + hl : (t / R) * R * hb + hl * R + (t % R);
   };
+  auto box_addr = [&](int row, int c) -> uint32_t {
+    return (uint32_t)((c >> 3) * blk + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+  };
+  const int k_key = mr + 8 * (mi & 1), v_key = mr + 8 * (mi >> 1);
+  const int k_row = boxed ? box_row(k_key) : 0, v_row = boxed ? box_row(v_key) : 0;
   const uint32_t sK0 = smem_u32(sK), sV0 = smem_u32(sV);
   const float sc = a.scale_log2;
   uint32_t it = 0, jc = 0;
@@ -561,11 +576,16 @@ __global__ void __launch_bounds__(320, 1)
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (F8) {
         // keys grp and grp + 8, dims 16ks + 4qd .. + 3 of each: one word each
+        // (chunk ks of the key's 128-byte row)
+        const int r0 = boxed ? box_row(grp) : 0, r1 = boxed ? box_row(grp + 8) : 0;
         const uint32_t k0 = kb + (uint32_t)(grp * RS + hl * D + 4 * qd);
         const uint32_t k1 = k0 + 8 * RS;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-          const uint32_t w0 = ld_shared_u32(k0 + 16 * ks), w1 = ld_shared_u32(k1 + 16 * ks);
+          const uint32_t w0 =
+              ld_shared_u32(boxed ? kb + box_addr(r0, ks) + 4 * qd : k0 + 16 * ks);
+          const uint32_t w1 =
+              ld_shared_u32(boxed ? kb + box_addr(r1, ks) + 4 * qd : k1 + 16 * ks);
           uint32_t af[4];
           af[0] = e4m3x2_to_f16x2(w0 & 0xffffu);
           af[1] = e4m3x2_to_f16x2(w1 & 0xffffu);
@@ -577,7 +597,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t af[4];
-          ldsm_x4(kb + (swz ? swz_addr(k_key, 2 * ks + (mi >> 1)) : k_lane + 32 * ks), af);
+          ldsm_x4(kb + (boxed ? box_addr(k_row, 2 * ks + (mi >> 1)) : k_lane + 32 * ks), af);
           mma16816(sacc, af, qf[ks][0], qf[ks][1]);
         }
       }
@@ -639,13 +659,17 @@ __global__ void __launch_bounds__(320, 1)
         // lanes per key, D / 2 codes each), then O^T += V^T . P^T from it
         const uint32_t vs = smem_u32(sVc) + (uint32_t)(hl * TS * vs_row_bytes(D));
         {
+          // keys past the tile (n < 16) may hold anything: they become zeros
           constexpr int PL = D / 2;  // codes per lane
           const int key = lane >> 1, half = lane & 1;
+          const int vrow = boxed ? box_row(key) : 0;
           const uint32_t src = vb + (uint32_t)(key * RS + hl * D + half * PL);
           const uint32_t dst = vs + (uint32_t)(key * vs_row_bytes(D) + half * PL * 2);
 #pragma unroll
           for (int x = 0; x < PL / 16; ++x) {
-            const uint4 c = ld_shared_v4(src + 16 * x);
+            uint4 c = ld_shared_v4(boxed ? vb + box_addr(vrow, half * (PL / 16) + x)
+                                         : src + 16 * x);
+            if (key >= n) c = make_uint4(0u, 0u, 0u, 0u);
             st_shared_v4(dst + 32 * x,
                          make_uint4(e4m3x2_to_f16x2(c.x & 0xffffu), e4m3x2_to_f16x2(c.x >> 16),
                                     e4m3x2_to_f16x2(c.y & 0xffffu), e4m3x2_to_f16x2(c.y >> 16)));
@@ -665,11 +689,20 @@ __global__ void __launch_bounds__(320, 1)
       } else {
         const uint32_t pb0 = transpose8x8(float2_to_bf16x2(p00, p01));
         const uint32_t pb1 = transpose8x8(float2_to_bf16x2(p10, p11));
-        // O^T += V^T . P^T
+        // O^T += V^T . P^T.  Keys past the tile (n < 16) may hold anything in
+        // the boxed layout: their V values become zeros (lane holds keys 2qd,
+        // 2qd + 1 in af[0], af[1] and keys 8 + 2qd, 9 + 2qd in af[2], af[3]).
+        const uint32_t vm0 = (2 * qd < n ? 0xffffu : 0u) | (2 * qd + 1 < n ? 0xffff0000u : 0u);
+        const uint32_t vm1 =
+            (2 * qd + 8 < n ? 0xffffu : 0u) | (2 * qd + 9 < n ? 0xffff0000u : 0u);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t af[4];
-          ldsm_x4_t(vb + (swz ? swz_addr(v_key, 2 * mt + (mi & 1)) : v_lane + 32 * mt), af);
+          ldsm_x4_t(vb + (boxed ? box_addr(v_row, 2 * mt + (mi & 1)) : v_lane + 32 * mt), af);
+          af[0] &= vm0;
+          af[1] &= vm0;
+          af[2] &= vm1;
+          af[3] &= vm1;
           mma16816(acc[mt], af, pb0, pb1);
         }
       }
@@ -771,32 +804,43 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// HND page pool {D, P, Hk, pages}: one box = min(P, 16) slots of one kv head
-// and 64 dims, 128-byte swizzle.
-bool encode_hnd(CUtensorMap* m, const void* base, const AttnArgs& a, int D) {
+// Boxed staging maps: NHD pool {D, Hk, P, pages} with box {128 B of columns,
+// hb heads, R slots, 1}; HND pool {D, P, Hk, pages} with box {128 B, R slots,
+// hb heads, 1}; R = min(P, 16); 128-byte swizzle.  Page ids come from
+// kv_indices, so the page dimension is declared as large as TMA allows.
+bool encode_box(CUtensorMap* m, const void* base, const AttnArgs& a, int D, int ES, int hb) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const uint64_t P = a.page_size, Hk = a.num_kv_heads;
-  cuuint64_t dims[4] = {(cuuint64_t)D, P, Hk, (cuuint64_t)1 << 31};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, P * D * 2, (cuuint64_t)a.page_stride * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)(P < (uint64_t)TS ? P : TS), 1, 1};
+  const cuuint64_t P = a.page_size, Hk = a.num_kv_heads, E = ES;
+  const cuuint32_t R = (cuuint32_t)(P < (cuuint64_t)TS ? P : TS), CW = 128 / ES;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  if (a.layout == PKA_NHD) {
+    dims[0] = D; dims[1] = Hk; dims[2] = P; dims[3] = (cuuint64_t)1 << 31;
+    strides[0] = D * E; strides[1] = Hk * D * E; strides[2] = (cuuint64_t)a.page_stride * E;
+    box[0] = CW; box[1] = (cuuint32_t)hb; box[2] = R; box[3] = 1;
+  } else {
+    dims[0] = D; dims[1] = P; dims[2] = Hk; dims[3] = (cuuint64_t)1 << 31;
+    strides[0] = D * E; strides[1] = P * D * E; strides[2] = (cuuint64_t)a.page_stride * E;
+    box[0] = CW; box[1] = R; box[2] = (cuuint32_t)hb; box[3] = 1;
+  }
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  return fn(m, ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, bool F8>
 cudaError_t launch_t(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+  constexpr int ES = F8 ? 1 : 2;
   const int hpc = a.heads_per_cta;
-  const bool swz = !F8 && use_swizzled(a.layout, a.page_size, a.kv_ragged);
   DecodeMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  if (swz && (!encode_hnd(&maps.k, a.k, a, D) || !encode_hnd(&maps.v, a.v, a, D)))
-    return cudaErrorInvalidValue;
-  const int stage_bytes =
-      2 * (swz ? hpc * (D / 64) * SWZ_BLK : TS * row_bytes(hpc, D, F8 ? 1 : 2));
+  int hb = use_boxes(a.page_size, a.kv_ragged, D, ES) ? box_heads(a.layout, hpc) : 0;
+  if (hb && (!encode_box(&maps.k, a.k, a, D, ES, hb) || !encode_box(&maps.v, a.v, a, D, ES, hb)))
+    hb = 0;  // fall back to one bulk copy per key row
+  const int stage_bytes = 2 * (hb ? (D * ES / 128) * TS * hb * 128 : TS * row_bytes(hpc, D, ES));
   const int scratch = F8 ? hpc * TS * vs_row_bytes(D) : 0;
   int stages = (kStageBudget - scratch) / stage_bytes;
   if (stages > (F8 ? kMaxStagesF8 : kMaxStages)) stages = F8 ? kMaxStagesF8 : kMaxStages;
@@ -807,7 +851,7 @@ cudaError_t launch_t(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, F8><<<num_ctas, 32 * (hpc + 2), smem, stream>>>(maps, a, stages);
+  decode_kernel<D, F8><<<num_ctas, 32 * (hpc + 2), smem, stream>>>(maps, a, stages, hb);
   return cudaGetLastError();
 }
 

@@ -152,7 +152,7 @@ def time_steps(fn, steps, warmup, stream, l2_buf=None):
 # Workloads
 # ---------------------------------------------------------------------------
 
-def decode_setup(device, kv_dtype="bf16"):
+def decode_setup(device, kv_dtype="bf16", on_tensor_cores=False):
     """Batch-decode workload; kv_dtype "e4m3" stores K/V as 8-bit codes (one
     scale per pool), halving the K/V bytes per key."""
     import paged_kv_attention_plan_gb300 as pka
@@ -164,7 +164,8 @@ def decode_setup(device, kv_dtype="bf16"):
              v=kv_tensor(b.v_pool, device), idx=i32(b.kv_indices, device))
     attn = pka.BatchAttention(device=device)
     kw = dict(num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16, split_mode="auto",
-              kv_dtype=kv_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
+              kv_dtype=kv_dtype, k_scale=b.k_scale, v_scale=b.v_scale,
+              decode_on_tensor_cores=on_tensor_cores)
     info = attn.plan(None, b.kv_indptr, b.last_page_len, **kw)
     d["attn"], d["info"] = attn, info
     t = []
@@ -460,8 +461,9 @@ def reference_arm(args, rank):
 
 def profile_one(name, device, stream, steps, warmup, pk):
     """Run one workload's steps only (used under ncu); prints its timings."""
-    if name in ("decode", "decode_fp8"):
-        d = decode_setup(device, "e4m3" if name == "decode_fp8" else "bf16")
+    if name in ("decode", "decode_fp8", "decode_tc"):
+        d = decode_setup(device, "e4m3" if name == "decode_fp8" else "bf16",
+                         on_tensor_cores=name == "decode_tc")
         ms = time_steps(lambda: decode_step(d), steps, warmup, stream)
         out = {"workload": "batch_decode", "ms": statistics.median(ms),
                "GB/s": d["bytes"] / (statistics.median(ms) * 1e-3) / 1e9}
@@ -494,8 +496,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "decode_fp8", "prefill",
-                                                          "ragged", "mixed1", "mixed16", "cascade"],
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "decode", "decode_fp8", "decode_tc", "prefill", "ragged",
+                             "mixed1", "mixed16", "cascade"],
                     help="all (default) prints the benchmark line; a single workload only runs "
                          "that workload's kernels (for profiling) and prints its numbers")
     args = ap.parse_args()
@@ -568,6 +571,16 @@ def main():
                                "frac": d8["bytes"] / (f8_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                "kernel": "decode_kernel<128, e4m3>"}}
     del d8
+    torch.cuda.empty_cache()
+    # ---- the same bf16 decode batch through the tensor-core (tcgen05) kernel
+    dt = decode_setup(device, on_tensor_cores=True)
+    tc_ms = statistics.median(time_steps(lambda: decode_step(dt), 200, 5, stream))
+    tc_decode = {"workload": "batch_decode rows on the tcgen05 kernel (decode_on_tensor_cores: "
+                             "one query token per item, the 4 qo heads of a kv head in the "
+                             "128-row tile)",
+                 "ms_per_step": tc_ms, "GB/s": dt["bytes"] / (tc_ms * 1e-3) / 1e9,
+                 "vs_decode_kernel": step_ms / tc_ms}
+    del dt
     torch.cuda.empty_cache()
 
     # ---- append + prefill (tensor cores)
@@ -660,7 +673,8 @@ def main():
                        "kv_bytes_per_step": d["kv_bytes"], "bytes_per_step": d["bytes"],
                        "l2": "inputs (604 MB of K/V) larger than L2; no flush",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roof, "fp8_kv_decode": fp8_decode, "prefill": prefill,
+            "roofline": roof, "fp8_kv_decode": fp8_decode, "tensor_core_decode": tc_decode,
+            "prefill": prefill,
             "ragged_custom_mask": ragged,
             "mixed_step": mixed, "cascade": cascade, "e2e": e2e,
             "gpu_launches": d["launches"] * args.steps,

@@ -108,7 +108,13 @@ typedef struct pka_params {
   int32_t kv_dtype;            /* pka_kv_dtype of the K/V pools                 */
   float k_scale;               /* PKA_KV_FP8_E4M3: scale of K codes (<= 0: 1)    */
   float v_scale;               /* PKA_KV_FP8_E4M3: scale of V codes (<= 0: 1)    */
-  int32_t reserved[2];         /* must be zero                                  */
+  /* 1: rows with qo_len == 1 also go to the tensor-core (tcgen05) kernel, the
+   * g qo heads of a row packed into its 128-row tile ("Deep Dive -
+   * FlashInfer": decode through the tensor-core tile for grouped heads);
+   * 0: they go to the decode kernel (warp-level MMAs, faster for decode on
+   * GB300).  bf16 K/V, no graph mode. */
+  int32_t decode_on_tensor_cores;
+  int32_t reserved[1];         /* must be zero                                  */
 } pka_params;
 
 /* Summary of a plan, filled by pka_plan (also when it fails with

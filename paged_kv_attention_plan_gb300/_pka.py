@@ -41,7 +41,8 @@ class pka_params(ctypes.Structure):
                 ("num_sms", ctypes.c_int32), ("graph_max_batch", ctypes.c_int32),
                 ("graph_max_qo_rows", ctypes.c_int32), ("graph_max_kv_tokens", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
-                ("v_scale", ctypes.c_float), ("reserved", ctypes.c_int32 * 2)]
+                ("v_scale", ctypes.c_float), ("decode_on_tensor_cores", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 1)]
 
 
 class pka_plan_info(ctypes.Structure):
@@ -187,7 +188,7 @@ def make_params(num_qo_heads, num_kv_heads, head_dim, page_size=1, layout="NHD",
                 mask_mode="causal", sm_scale=0.0, kv_ragged=False, split_mode="auto",
                 fixed_split_pages=1, num_sms=0, graph_max_batch=0, graph_max_qo_rows=0,
                 graph_max_kv_tokens=0, kv_dtype="bf16", k_scale=1.0,
-                v_scale=1.0) -> pka_params:
+                v_scale=1.0, decode_on_tensor_cores=False) -> pka_params:
     p = pka_params()
     p.num_qo_heads, p.num_kv_heads, p.head_dim = num_qo_heads, num_kv_heads, head_dim
     p.page_size = page_size
@@ -206,6 +207,7 @@ def make_params(num_qo_heads, num_kv_heads, head_dim, page_size=1, layout="NHD",
     p.kv_dtype = ({"bf16": PKA_KV_BF16, "e4m3": PKA_KV_FP8_E4M3}[kv_dtype]
                   if isinstance(kv_dtype, str) else kv_dtype)
     p.k_scale, p.v_scale = k_scale, v_scale
+    p.decode_on_tensor_cores = int(bool(decode_on_tensor_cores))
     return p
 
 

@@ -47,8 +47,8 @@ pka_status cuda_fail(cudaError_t e, const char* where) {
 
 bool params_ok(const pka_params* p) {
   if (!p) return false;
-  for (int i = 0; i < 2; ++i)
-    if (p->reserved[i] != 0) return false;
+  if (p->reserved[0] != 0) return false;
+  if (p->decode_on_tensor_cores != 0 && p->decode_on_tensor_cores != 1) return false;
   if (p->graph_max_batch < 0 || p->graph_max_qo_rows < 0 || p->graph_max_kv_tokens < 0)
     return false;
   if (p->graph_max_batch == 0 && (p->graph_max_qo_rows || p->graph_max_kv_tokens)) return false;
@@ -73,6 +73,8 @@ pka_status check_supported(const pka_params* p) {
   if (g != 1 && g != 2 && g != 4 && g != 8) return PKA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128) return PKA_ERR_UNSUPPORTED;
   if (p->graph_max_batch > 0 && p->split_mode == PKA_SPLIT_FIXED) return PKA_ERR_UNSUPPORTED;
+  if (p->decode_on_tensor_cores && (p->graph_max_batch > 0 || p->kv_dtype != PKA_KV_BF16))
+    return PKA_ERR_UNSUPPORTED;
   return PKA_OK;
 }
 
@@ -340,7 +342,7 @@ void plan_decode(const pka_params* p, const std::vector<Batch>& lv, int num_sms,
   for (int l = 0; l < (int)lv.size(); ++l) {
     const Batch& b = lv[l];
     for (int r = 0; r < (int)b.qo_len.size(); ++r) {
-      if (b.qo_len[r] != 1) continue;
+      if (b.qo_len[r] != 1 || p->decode_on_tensor_cores) continue;
       if (L->cascade && b.kv_len[r] == 0) continue;  // an empty node adds no state
       for (int hg = 0; hg < hg_count; ++hg) {
         units.push_back({l, r, hg, b.kv_len[r]});
@@ -422,7 +424,7 @@ void plan_prefill(const pka_params* p, const std::vector<Batch>& lv, int num_sms
     const Batch& b = lv[l];
     for (int r = 0; r < (int)b.qo_len.size(); ++r) {
       int Q = b.qo_len[r], K = b.kv_len[r];
-      if (Q < 2) continue;
+      if (Q < (p->decode_on_tensor_cores ? 1 : 2)) continue;
       if (L->cascade && K == 0) continue;  // an empty node adds no state
       for (int h = 0; h < p->num_kv_heads; ++h)
         for (int q0 = 0; q0 < Q; q0 += tq) {

@@ -35,14 +35,14 @@ def i32(a, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
 
 
-def run_gpu(b, split=("auto", 1), packed_mask=None, attn=None, with_lse=True):
+def run_gpu(b, split=("auto", 1), packed_mask=None, attn=None, with_lse=True, **plan_kw):
     attn = attn or pka.BatchAttention()
     qo = None if b.is_decode else b.qo_indptr
     info = attn.plan(qo, b.kv_indptr, b.last_page_len, num_qo_heads=b.num_qo_heads,
                      num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size,
                      layout=b.layout, mask_mode=b.mask_mode, kv_ragged=b.kv_ragged,
                      split_mode=split[0], fixed_split_pages=split[1], kv_dtype=b.kv_dtype,
-                     k_scale=b.k_scale, v_scale=b.v_scale)
+                     k_scale=b.k_scale, v_scale=b.v_scale, **plan_kw)
     q = bf16(b.q)
     k, v = kv_tensor(b.k_pool), kv_tensor(b.v_pool)
     idx = i32(b.kv_indices)

@@ -79,7 +79,10 @@ def test_validate_rejections(qo, kv, last, params, want):
 
 def test_reserved_fields_must_be_zero():
     p = _p()
-    p.reserved[1] = 1
+    p.reserved[0] = 1
+    assert pka.pka_validate(p, *WORKED) == INVALID
+    p = _p()
+    p.decode_on_tensor_cores = 2
     assert pka.pka_validate(p, *WORKED) == INVALID
 
 
@@ -332,3 +335,39 @@ def test_fp8_kv_is_decode_only():
     bad.kv_dtype = 7
     assert pka.pka_plan(pka.pka_plan_create(), bad, None, b.kv_indptr, b.last_page_len, None,
                         buf, check=False) == INVALID
+
+
+@pytest.mark.parametrize("cfg", ["worked", "decode", "mixed_p16_hnd"])
+def test_decode_rows_on_tensor_cores_plan(cfg):
+    """With decode_on_tensor_cores, rows with qo_len == 1 become tensor-core
+    items (one query token, the g heads of each kv head packed into the tile)
+    whose key ranges tile [0, kv_len) per (request, kv head); the decode list
+    is empty.  Graph mode and e4m3 K/V refuse the option."""
+    b = CONFIGS[cfg]()
+    hq, hk = b.num_qo_heads, b.num_kv_heads
+    params = pka.make_params(hq, hk, b.head_dim, b.page_size, b.layout, b.mask_mode,
+                             num_sms=152, decode_on_tensor_cores=True)
+    h = pka.pka_plan_create()
+    buf = np.zeros(1 << 24, np.uint8)
+    qo = None if b.is_decode else b.qo_indptr
+    assert pka.pka_plan(h, params, qo, b.kv_indptr, b.last_page_len, None, buf, check=False) == OK
+    info = pka.pka_plan_get_info(h)
+    pka.pka_plan_destroy(h)
+    plan = parse(buf)
+    assert info.num_decode_items == 0 and not plan["decode_items"]
+    qo_len = np.diff(b.qo_indptr)
+    units = {}
+    for it in plan["prefill_items"]:
+        units.setdefault((it["req"], it["kv_head0"], it["q_local0"]), []).append(it)
+    for r in np.nonzero(qo_len == 1)[0]:
+        for kh in range(hk):
+            its = units[(int(r), kh, 0)]
+            assert all(i["q_count"] == 1 for i in its)
+            assert _ranges_tile([(i["t0"], i["t1"]) for i in its], int(b.kv_lens[r]))
+    g = pka.make_params(hq, hk, b.head_dim, b.page_size, b.layout, b.mask_mode,
+                        decode_on_tensor_cores=True, graph_max_batch=len(b.kv_lens),
+                        graph_max_qo_rows=int(b.nnz_q))
+    assert pka.pka_validate(g, b.qo_indptr, b.kv_indptr, b.last_page_len) == UNSUPPORTED
+    f = pka.make_params(hq, hk, b.head_dim, b.page_size, b.layout, b.mask_mode,
+                        decode_on_tensor_cores=True, kv_dtype="e4m3")
+    assert pka.pka_validate(f, b.qo_indptr, b.kv_indptr, b.last_page_len) == UNSUPPORTED

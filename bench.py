@@ -569,6 +569,7 @@ def main():
                   "roofline": {"bound": "hbm", "achieved": d8["bytes"] / (f8_ms * 1e-3) / 1e9,
                                "peak": pk["hbm_gbs"], "unit": "GB/s",
                                "frac": d8["bytes"] / (f8_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                               "traffic": recorded_traffic("decode_kernel<128, e4m3>"),
                                "kernel": "decode_kernel<128, e4m3>"}}
     del d8
     torch.cuda.empty_cache()

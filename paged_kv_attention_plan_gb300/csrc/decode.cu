@@ -659,9 +659,11 @@ __global__ void __launch_bounds__(320, 1)
         // lanes per key, D / 2 codes each), then O^T += V^T . P^T from it
         const uint32_t vs = smem_u32(sVc) + (uint32_t)(hl * TS * vs_row_bytes(D));
         {
-          // keys past the tile (n < 16) may hold anything: they become zeros
+          // keys past the tile (n < 16) may hold anything: they become zeros.
+          // Lane = key + 16 * half: each group of 8 lanes stores 8 different
+          // keys' rows, whose starts fall in 8 different bank groups.
           constexpr int PL = D / 2;  // codes per lane
-          const int key = lane >> 1, half = lane & 1;
+          const int key = lane & 15, half = lane >> 4;
           const int vrow = boxed ? box_row(key) : 0;
           const uint32_t src = vb + (uint32_t)(key * RS + hl * D + half * PL);
           const uint32_t dst = vs + (uint32_t)(key * vs_row_bytes(D) + half * PL * 2);

@@ -401,11 +401,8 @@ __global__ void __launch_bounds__(320, 1)
 
   const int i0 = a.cta_ptr[blockIdx.x], i1 = a.cta_ptr[blockIdx.x + 1];
   if (i0 >= i1) return;  // an empty CTA of a fixed (graph mode) grid
-  // Rows of a partial tile that no copy writes must hold finite values (their
-  // P is 0, and 0 * NaN would poison O): zero the stages once.
-  for (int x = threadIdx.x; x < 2 * stages * stage_bytes / 16; x += blockDim.x)
-    reinterpret_cast<uint4*>(smem)[x] = make_uint4(0, 0, 0, 0);
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  // Rows of a tile past its last key are never zeroed in shared memory: their
+  // scores are replaced by -inf and their V values by zeros in registers.
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(bars.full(s), 33);  // expect_tx by lane 0 + the 32 producer lanes

@@ -78,6 +78,31 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     return np.where((e == 15) & (c & 7 == 7), np.nan, out)
 
 
+def f32_to_e4m3(x) -> np.ndarray:
+    """Round float32 values to e4m3 codes: to the nearest value of the format
+    (ties to the even code, the one whose lowest mantissa bit is 0), with
+    magnitudes above the largest finite value 448 clamped to 448 (saturating:
+    nothing finite becomes NaN) and NaN kept as the NaN code 0x7F."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    pos_codes = np.arange(0, 0x7F, dtype=np.uint8)  # +0 .. 448, increasing values
+    pos_vals = e4m3_to_f64(pos_codes)
+    a = np.minimum(np.abs(np.nan_to_num(x)), 448.0)
+    hi = np.clip(np.searchsorted(pos_vals, a, side="left"), 0, len(pos_vals) - 1)
+    lo = np.clip(hi - 1, 0, len(pos_vals) - 1)
+    d_lo, d_hi = a - pos_vals[lo], pos_vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (pos_codes[hi] % 2 == 0))
+    code = np.where(pick_hi, pos_codes[hi], pos_codes[lo]).astype(np.uint8)
+    code = np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def quantize_kv_e4m3(bits: np.ndarray, scale: float) -> np.ndarray:
+    """bf16 payload -> e4m3 codes of value / scale: the division in float32
+    (correctly rounded), then the one rounding to e4m3 (f32_to_e4m3)."""
+    v = bf16_bits_to_f64(bits).astype(np.float32)
+    return f32_to_e4m3(v / np.float32(scale))
+
+
 def kv_payload_to_f64(x, kv_dtype: str, scale: float) -> np.ndarray:
     """K or V payload as float64 values: bf16 bit patterns, or e4m3 codes
     times the pool's scale."""
@@ -422,12 +447,17 @@ def cascade_attention(q_bits, k_pool_bits, v_pool_bits, *, levels, page_size, nu
 # ---------------------------------------------------------------------------
 
 def append_paged_kv_cache(k_new, v_new, append_indptr, k_pool, v_pool, *, kv_indptr, kv_indices,
-                          last_page_len, page_size, layout="NHD"):
+                          last_page_len, page_size, layout="NHD", kv_dtype="bf16", k_scale=1.0,
+                          v_scale=1.0):
     """Return copies of the pools with the appended rows written.
 
     Request r appends rows append_indptr[r]..append_indptr[r+1]; its KV length
     (from the CSR page table) already counts them, so appended token t lands at
-    logical position kv_len - n_append + t."""
+    logical position kv_len - n_append + t.  e4m3 pools receive each bf16 value
+    divided by the pool's scale, rounded to e4m3 (quantize_kv_e4m3)."""
+    if kv_dtype == "e4m3":
+        k_new = quantize_kv_e4m3(k_new, k_scale)
+        v_new = quantize_kv_e4m3(v_new, v_scale)
     k_out = np.array(k_pool, copy=True)
     v_out = np.array(v_pool, copy=True)
     kv_lens = kv_lens_from_csr(kv_indptr, kv_indices, last_page_len, page_size)

@@ -101,3 +101,70 @@ def test_unused_slots_are_nan_codes():
                            is_decode=True, kv_dtype="e4m3")
     assert b.k_pool.dtype == np.uint8
     assert np.isnan(ref.e4m3_to_f64(b.k_pool)).any()  # any over-read would poison a result
+
+
+# ---------------------------------------------------------------------------
+# Quantization to e4m3 (appends into e4m3 pools)
+# ---------------------------------------------------------------------------
+
+def _midpoints():
+    v = ref.e4m3_to_f64(np.arange(0, 0x7F, dtype=np.uint8))
+    return ((v[:-1] + v[1:]) / 2).astype(np.float32)
+
+
+def test_quantize_round_trips_every_finite_code():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = ref.e4m3_to_f64(codes)
+    fin = ~np.isnan(vals)
+    assert np.array_equal(ref.f32_to_e4m3(vals[fin].astype(np.float32)), codes[fin])
+
+
+def test_quantize_matches_torch_within_range():
+    """PyTorch's float8_e4m3fn cast rounds to nearest even; the two agree
+    wherever PyTorch does not overflow (|x| <= 464, the midpoint above 448)."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this PyTorch")
+    rng = np.random.default_rng(11)
+    x = np.concatenate([
+        (rng.standard_normal(20000) * np.exp2(rng.integers(-12, 9, 20000))).astype(np.float32),
+        _midpoints(), -_midpoints(),                       # exact ties
+        np.float32([0.0, -0.0, 2.0 ** -10, 448.0, 464.0, -464.0])])
+    x = x[np.abs(x) <= 464.0]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ref.f32_to_e4m3(x), want)
+
+
+def test_quantize_saturates_and_keeps_nan():
+    x = np.float32([465.0, 1e6, np.inf, -500.0, -np.inf, np.nan])
+    assert list(ref.f32_to_e4m3(x)) == [0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F]
+
+
+def test_planted_ties_away_from_zero_fails():
+    mids = _midpoints()
+    good = ref.f32_to_e4m3(mids)
+    v = ref.e4m3_to_f64(np.arange(0, 0x7F, dtype=np.uint8))
+    away = np.searchsorted(v, mids.astype(np.float64), side="left").astype(np.uint8)
+    assert not np.array_equal(good, away)
+
+
+def test_quantizing_append_round_trip():
+    """Appending bf16 rows into e4m3 pools stores round(value / scale); reading
+    the pools back (the attention gather) yields the decoded codes times the
+    scale, and untouched (NaN-coded) slots stay as they were."""
+    b = W.make_paged_batch(12, [3, 1, 5], [7, 2, 9], page_size=4, hq=4, hk=2, d=64,
+                           append_new=True)
+    k8 = np.full(b.k_pool.shape, W.E4M3_NAN_CODE, np.uint8)
+    v8 = np.full(b.v_pool.shape, W.E4M3_NAN_CODE, np.uint8)
+    ko, vo = ref.append_paged_kv_cache(b.k_new, b.v_new, b.qo_indptr, k8, v8,
+                                       kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+                                       last_page_len=b.last_page_len, page_size=4,
+                                       kv_dtype="e4m3", k_scale=0.25, v_scale=3.0)
+    want_k = ref.quantize_kv_e4m3(b.k_new, 0.25)
+    for r in range(3):
+        q0, q1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
+        rows = ref.gather_request_kv(ko, layout="NHD", page_size=4, kv_indptr=b.kv_indptr,
+                                     kv_indices=b.kv_indices, req=r, kv_len=int(b.kv_lens[r]))
+        assert np.array_equal(rows[-(q1 - q0):], want_k[q0:q1])
+    touched = ko != W.E4M3_NAN_CODE
+    assert touched.sum() <= b.k_new.size and (vo != W.E4M3_NAN_CODE).sum() <= b.v_new.size

@@ -249,7 +249,11 @@ pka_status pka_run(pka_plan_t plan, const pka_params* params, const void* q, con
  *   last_page_len_d) already counts them, so row t lands at logical position
  *   kv_len - n_append + t.  Uses params->num_kv_heads, head_dim, page_size and
  *   layout.  Device metadata is trusted (not validated); nnz_new must equal
- *   append_indptr_d[batch].  bf16 pools only (PKA_ERR_UNSUPPORTED for e4m3). */
+ *   append_indptr_d[batch].  k_new / v_new are bf16; e4m3 pools
+ *   (params->kv_dtype) store each value divided by k_scale / v_scale, rounded
+ *   to the nearest e4m3 value (ties to even), magnitudes above 448 clamped to
+ *   448.  Buffers 16-byte aligned, page_stride a multiple of 16 bytes;
+ *   PKA_ERR_INVALID_ARG otherwise. */
 pka_status pka_append_paged_kv_cache(const pka_params* params, int32_t batch, const void* k_new,
                                      const void* v_new, const int32_t* append_indptr_d,
                                      int64_t nnz_new, const int32_t* kv_indptr_d,

@@ -60,7 +60,7 @@ cudaError_t launch_packbits(const uint8_t* in, int64_t n, uint8_t* out, cudaStre
 cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_new,
                           const uint16_t* v_new, const int32_t* append_indptr, int64_t nnz,
                           const int32_t* kv_indptr, const int32_t* kv_indices,
-                          const int32_t* last_page_len, uint16_t* k, uint16_t* v,
+                          const int32_t* last_page_len, void* k, void* v,
                           int64_t page_stride, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
 // Device address of the error word on the current device (null on failure).

@@ -901,17 +901,22 @@ pka_status pka_append_paged_kv_cache(const pka_params* p, int32_t batch, const v
                                      void* k, void* v, int64_t page_stride, void* stream) {
   if (!params_ok(p) || batch < 0 || nnz_new < 0) return PKA_ERR_INVALID_ARG;
   if (p->head_dim != 64 && p->head_dim != 128) return PKA_ERR_UNSUPPORTED;
-  if (p->kv_dtype != PKA_KV_BF16) return PKA_ERR_UNSUPPORTED;  // no quantizing append
+
   if (p->kv_ragged) return PKA_ERR_UNSUPPORTED;
   if (nnz_new == 0 || batch == 0) return PKA_OK;
   if (!k_new || !v_new || !append_indptr || !kv_indptr || !kv_indices || !last_page_len || !k ||
       !v || page_stride <= 0)
     return PKA_ERR_INVALID_ARG;
+  // 16-byte row pieces move per thread: 16-byte aligned buffers, and a page
+  // stride of whole 16-byte units (8 bf16 or 16 e4m3 elements)
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+                        reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v);
+  if ((mis & 15) || (page_stride & (p->kv_dtype == PKA_KV_FP8_E4M3 ? 15 : 7)))
+    return PKA_ERR_INVALID_ARG;
   cudaError_t e = pka::launch_append(*p, batch, static_cast<const uint16_t*>(k_new),
                                      static_cast<const uint16_t*>(v_new), append_indptr, nnz_new,
-                                     kv_indptr, kv_indices, last_page_len,
-                                     static_cast<uint16_t*>(k), static_cast<uint16_t*>(v),
-                                     page_stride, static_cast<cudaStream_t>(stream));
+                                     kv_indptr, kv_indices, last_page_len, k, v, page_stride,
+                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKA_OK : cuda_fail(e, "append launch");
 }
 

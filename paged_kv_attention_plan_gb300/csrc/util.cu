@@ -158,12 +158,32 @@ __global__ void __launch_bounds__(256) packbits_kernel(const uint8_t* __restrict
 // 16 bytes of K and of V; the request of a row comes from a binary search of
 // append_indptr.
 // ---------------------------------------------------------------------------
+// e4m3 pools: 8 values, each divided by the pool's scale (correctly rounded
+// float32 division), then rounded to nearest even e4m3 with saturation at the
+// largest finite value (cvt .satfinite), 8 codes packed little-endian.
+__device__ __forceinline__ uint2 bf16x8_to_e4m3x8(uint4 x, float scale) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t pk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = bf16x2_to_float2(w[i]);
+    const float lo = __fdiv_rn(f.x, scale), hi = __fdiv_rn(f.y, scale);
+    uint32_t r;
+    asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n cvt.u32.u16 %0, t;\n}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    pk[i] = r;
+  }
+  return make_uint2(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16));
+}
+
+template <bool F8>
 __global__ void __launch_bounds__(256) append_kernel(
     const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
     const int32_t* __restrict__ append_indptr, int32_t batch, int64_t nnz,
     const int32_t* __restrict__ kv_indptr, const int32_t* __restrict__ kv_indices,
-    const int32_t* __restrict__ last_page_len, uint16_t* __restrict__ k,
-    uint16_t* __restrict__ v, int64_t page_stride, int hk, int d, int P, int layout) {
+    const int32_t* __restrict__ last_page_len, void* __restrict__ k, void* __restrict__ v,
+    int64_t page_stride, int hk, int d, int P, int layout, float k_scale, float v_scale) {
   const int vec_per_head = d / 8;
   const int64_t vec_per_row = (int64_t)hk * vec_per_head;
   const int64_t total = nnz * vec_per_row;
@@ -189,8 +209,15 @@ __global__ void __launch_bounds__(256) append_kernel(
     dst += layout == PKA_NHD ? ((int64_t)slot * hk + h) * d : ((int64_t)h * P + slot) * d;
     dst += c * 8;
     const int64_t src = (row * hk + h) * d + c * 8;
-    *reinterpret_cast<uint4*>(k + dst) = *reinterpret_cast<const uint4*>(k_new + src);
-    *reinterpret_cast<uint4*>(v + dst) = *reinterpret_cast<const uint4*>(v_new + src);
+    const uint4 kx = *reinterpret_cast<const uint4*>(k_new + src);
+    const uint4 vx = *reinterpret_cast<const uint4*>(v_new + src);
+    if constexpr (F8) {  // element offsets are byte offsets in e4m3 pools
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(k) + dst) = bf16x8_to_e4m3x8(kx, k_scale);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(v) + dst) = bf16x8_to_e4m3x8(vx, v_scale);
+    } else {
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(k) + dst) = kx;
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(v) + dst) = vx;
+    }
   }
 }
 
@@ -221,12 +248,18 @@ cudaError_t launch_packbits(const uint8_t* in, int64_t n, uint8_t* out, cudaStre
 cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_new,
                           const uint16_t* v_new, const int32_t* append_indptr, int64_t nnz,
                           const int32_t* kv_indptr, const int32_t* kv_indices,
-                          const int32_t* last_page_len, uint16_t* k, uint16_t* v,
+                          const int32_t* last_page_len, void* k, void* v,
                           int64_t page_stride, cudaStream_t stream) {
   const int64_t work = nnz * p.num_kv_heads * (p.head_dim / 8);
-  append_kernel<<<grid_for(work, 256), 256, 0, stream>>>(
-      k_new, v_new, append_indptr, batch, nnz, kv_indptr, kv_indices, last_page_len, k, v,
-      page_stride, p.num_kv_heads, p.head_dim, p.page_size, p.layout);
+  const float ks = p.k_scale > 0.f ? p.k_scale : 1.f, vs = p.v_scale > 0.f ? p.v_scale : 1.f;
+  if (p.kv_dtype == PKA_KV_FP8_E4M3)
+    append_kernel<true><<<grid_for(work, 256), 256, 0, stream>>>(
+        k_new, v_new, append_indptr, batch, nnz, kv_indptr, kv_indices, last_page_len, k, v,
+        page_stride, p.num_kv_heads, p.head_dim, p.page_size, p.layout, ks, vs);
+  else
+    append_kernel<false><<<grid_for(work, 256), 256, 0, stream>>>(
+        k_new, v_new, append_indptr, batch, nnz, kv_indptr, kv_indices, last_page_len, k, v,
+        page_stride, p.num_kv_heads, p.head_dim, p.page_size, p.layout, 1.f, 1.f);
   return cudaGetLastError();
 }
 

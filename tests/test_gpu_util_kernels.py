@@ -50,6 +50,70 @@ def test_append_bit_exact_full_size():
     assert np.array_equal(k, k_ref) and np.array_equal(v, v_ref)
 
 
+def _fp8_pools(b, seed):
+    """e4m3 pools of the batch's shape holding random codes everywhere; the
+    append overwrites its own slots."""
+    rng = np.random.default_rng(seed)
+    k8 = W.e4m3_codes(rng, b.k_pool.shape)
+    v8 = W.e4m3_codes(rng, b.v_pool.shape)
+    return k8, v8
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("page_size,d,scales", [(1, 64, (1.0, 1.0)), (4, 128, (0.3, 2.5)),
+                                                (16, 128, (0.004, 0.75))])
+def test_append_into_e4m3_pools_bit_exact(layout, page_size, d, scales):
+    """bf16 rows appended into e4m3 pools: value / scale rounded to nearest
+    even e4m3, saturating (k_scale 0.004 drives most values past 448)."""
+    b = W.make_paged_batch(60 + page_size, [3, 1, 0, 17, 40], [6, 2, 5, 40, 41],
+                           page_size=page_size, layout=layout, hq=8, hk=2, d=d, append_new=True)
+    k8, v8 = _fp8_pools(b, page_size)
+    params = pka.make_params(8, 2, d, page_size, layout, kv_dtype="e4m3", k_scale=scales[0],
+                             v_scale=scales[1])
+    k, v = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
+    pka.pka_append_paged_kv_cache(params, bf16(b.k_new), bf16(b.v_new), i32(b.qo_indptr),
+                                  i32(b.kv_indptr), i32(b.kv_indices), i32(b.last_page_len), k,
+                                  v, k.stride(0))
+    torch.cuda.synchronize()
+    k_ref, v_ref = ref.append_paged_kv_cache(b.k_new, b.v_new, b.qo_indptr, k8, v8,
+                                             kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+                                             last_page_len=b.last_page_len, page_size=page_size,
+                                             layout=layout, kv_dtype="e4m3", k_scale=scales[0],
+                                             v_scale=scales[1])
+    assert np.array_equal(k.cpu().numpy(), k_ref) and np.array_equal(v.cpu().numpy(), v_ref)
+    if scales[0] < 0.01:
+        assert (k_ref == 0x7E).any() or (k_ref == 0xFE).any()  # saturation was exercised
+
+
+def test_append_then_decode_e4m3():
+    """A decode step over e4m3 pools whose newest token was just appended from
+    bf16: the oracle quantizes the same way and decodes the codes."""
+    b = W.make_paged_batch(70, [1, 1, 1], [33, 70, 16], page_size=16, hq=32, hk=8, d=128,
+                           append_new=True, is_decode=True)
+    k8, v8 = _fp8_pools(b, 7)
+    params = pka.make_params(32, 8, 128, 16, kv_dtype="e4m3", k_scale=0.5, v_scale=1.5)
+    k, v = torch.from_numpy(k8).cuda(), torch.from_numpy(v8).cuda()
+    pka.pka_append_paged_kv_cache(params, bf16(b.k_new), bf16(b.v_new), i32(b.qo_indptr),
+                                  i32(b.kv_indptr), i32(b.kv_indices), i32(b.last_page_len), k,
+                                  v, k.stride(0))
+    attn = pka.BatchAttention()
+    attn.plan(None, b.kv_indptr, b.last_page_len, num_qo_heads=32, num_kv_heads=8, head_dim=128,
+              page_size=16, kv_dtype="e4m3", k_scale=0.5, v_scale=1.5)
+    o, lse = attn.run(bf16(b.q), k, v, i32(b.kv_indices))
+    torch.cuda.synchronize()
+    k_ref, v_ref = ref.append_paged_kv_cache(b.k_new, b.v_new, b.qo_indptr, k8, v8,
+                                             kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+                                             last_page_len=b.last_page_len, page_size=16,
+                                             kv_dtype="e4m3", k_scale=0.5, v_scale=1.5)
+    o_ref, lse_ref = ref.batch_attention(b.q, k_ref, v_ref, qo_indptr=b.qo_indptr,
+                                         kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+                                         last_page_len=b.last_page_len, page_size=16,
+                                         num_qo_heads=32, num_kv_heads=8, kv_dtype="e4m3",
+                                         k_scale=0.5, v_scale=1.5)
+    from tests.gpu_util import assert_parity
+    assert_parity(f64(o), f64(lse), o_ref, lse_ref)
+
+
 @pytest.mark.parametrize("dim", [64, 128])
 def test_merge_states_matches_oracle(dim):
     rng = np.random.default_rng(dim)

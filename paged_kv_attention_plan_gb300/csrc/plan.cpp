@@ -302,10 +302,12 @@ void order_split_pieces(PlanLists* L) {
   const int ctas = (int)ptr.size() - 1;
   for (int c = 0; c < ctas; ++c)
     if (ptr[c + 1] - ptr[c] == 1 && items[ptr[c]].join >= 0) ++ends[items[ptr[c]].join];
+  std::vector<PkaWorkItem> split, whole;
   for (int c = 0; c < ctas; ++c) {
     const int b = ptr[c], e = ptr[c + 1];
     if (e - b < 2) continue;
-    std::vector<PkaWorkItem> split, whole;
+    split.clear();
+    whole.clear();
     for (int i = b; i < e; ++i) (items[i].join >= 0 ? split : whole).push_back(items[i]);
     if (split.empty()) continue;
     if (!whole.empty()) {
@@ -361,10 +363,12 @@ void plan_decode(const pka_params* p, const std::vector<Batch>& lv, int num_sms,
   }
   L->decode_chunk = (int)chunk;
   auto& items = L->dec_items;
+  std::vector<int> pieces;  // items of the current unit (reused: the planner runs every step)
+  pieces.reserve(64);
   if (p->split_mode != PKA_SPLIT_AUTO) {
     // one CTA per piece
     for (const Unit& u : units) {
-      std::vector<int> pieces;
+      pieces.clear();
       int64_t step = chunk > 0 ? chunk : std::max(u.K, 1);
       int64_t t = 0;
       do {
@@ -378,9 +382,12 @@ void plan_decode(const pka_params* p, const std::vector<Batch>& lv, int num_sms,
     }
     return;
   }
+  items.reserve(units.size() + 2 * (size_t)num_sms + 2);
+  L->dec_cta_ptr.reserve(2 * (size_t)num_sms + 2);
+  L->joins.reserve(units.size() * hpc);
   int64_t load = 0;
   for (const Unit& u : units) {
-    std::vector<int> pieces;
+    pieces.clear();
     int64_t t = 0;
     do {
       // Cuts inside a request fall on 16-key tile boundaries, so that whole

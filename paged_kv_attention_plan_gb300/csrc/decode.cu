@@ -22,14 +22,14 @@
 // state.  The pieces of a split request count themselves in a join counter
 // of the plan image, and the last one merges the pieces' states ("A worked
 // split-KV example") and writes O and the LSE, so no separate merge launch
-// follows the decode kernel.  A consumer warp that finds (from a read of the
-// counter during its last tile) that every other piece has finished merges
-// them with its own state in registers.  Otherwise it writes its partial
-// state.  For a CTA's last item it then counts the piece in itself, and
-// merges from the workspace if that completes the count (each warp its own
-// kv head, in parallel).  Earlier split pieces go to the CTA's join warp,
-// which makes their states visible GPU-wide and counts them in while the
-// consumers go on with the next item.
+// follows the decode kernel.  Every piece writes its partial state.  A
+// consumer warp that finds (from a read of the counter during its last tile)
+// that every other piece has finished then merges all the pieces' states.
+// Otherwise, for a CTA's last item it counts the piece in itself and merges
+// if that completes the count (each warp its own kv head, in parallel);
+// earlier split pieces go to the CTA's join warp, which makes their states
+// visible GPU-wide and counts them in while the consumers go on with the next
+// item.
 //
 // e4m3 K/V (8-bit codes with one scale per pool) stages half the bytes per
 // key.  K fragments come straight from shared memory: one 32-bit load holds
@@ -51,9 +51,12 @@
 // are consecutive rows.  An NHD box is [slots][heads]; its head count is
 // rounded up to an odd number (the extra head lies past the pool's last head
 // and is zero-filled, or belongs to the next head block), so that a head's
-// 8 consecutive keys fall in 8 different swizzle phases.  A tile's last keys
-// may lie past the request's end inside its last page: their scores are
-// replaced by -inf and their V rows by zeros before the P V product.
+// 8 consecutive keys fall in 8 different swizzle phases.
+//
+// In either layout the rows of a tile past its last key hold whatever the
+// stage held before (or, boxed, the rest of the request's last page): their
+// scores are replaced by -inf and their V values by zeros in registers
+// before the P V product, so shared memory is never cleared.
 #include <cudaTypedefs.h>
 
 #include <cstring>

@@ -229,6 +229,8 @@ pka_status pka_plan_wait(pka_plan_t plan);
  *   kv_indices_d are ignored.
  *   packed_mask_d: little-endian bit array, read only for PKA_MASK_CUSTOM.
  *   float_ws_d: at least info.float_ws_bytes (may be NULL when that is 0).
+ *   A plan without query rows (info.nnz_qo == 0, not graph mode) returns
+ *   PKA_OK at once; its buffers may be NULL.
  *   Split decode rows are merged inside the decode kernel: each piece counts
  *   itself in a counter of the device plan image, and the last one merges.
  *   The counters return to zero by the end of every run, so one plan serves

@@ -820,6 +820,9 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
   if (!plan || !p || !plan->planned) return PKA_ERR_INVALID_ARG;
   if (std::memcmp(&plan->params, p, sizeof(pka_params)) != 0) return PKA_ERR_STALE_PLAN;
   if (!plan->int_ws_d) return PKA_ERR_INVALID_ARG;  // a host-only (dry-run) plan cannot run
+  // no query rows (an empty batch, or only qo_len == 0 requests): nothing to
+  // compute, and the (empty) buffers may be null
+  if (plan->info.nnz_qo == 0 && !graph_mode(p)) return PKA_OK;
   if (!q || !k || !v || !o) return PKA_ERR_INVALID_ARG;
   if (!p->kv_ragged && (!kv_indices || page_stride <= 0)) return PKA_ERR_INVALID_ARG;
   // 16-byte alignment of every row the kernels move with vector or bulk copies

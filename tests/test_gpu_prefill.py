@@ -212,3 +212,19 @@ def test_output_only_16_byte_aligned(d):
     o, lse = attn.run(bf16(b.q), bf16(b.k_pool), bf16(b.v_pool), i32(b.kv_indices), out=out)
     torch.cuda.synchronize()
     assert_parity(f64(o), f64(lse), *run_oracle(b))
+
+
+@pytest.mark.parametrize("qo,kv,last", [([0], [0], []), ([0, 0, 0], [0, 2, 3], [3, 1])])
+def test_run_without_query_rows(qo, kv, last):
+    """Empty batches run without launching anything, with empty (null) buffers."""
+    attn = pka.BatchAttention()
+    info = attn.plan(np.asarray(qo, np.int32), np.asarray(kv, np.int32),
+                     np.asarray(last, np.int32), num_qo_heads=8, num_kv_heads=2, head_dim=64,
+                     page_size=4)
+    assert info.nnz_qo == 0
+    q = torch.empty((0, 8, 64), dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros((4, 4, 2, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = attn.run(q, pool, pool, torch.zeros(3, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert o.shape == (0, 8, 64) and lse.shape == (0, 8)
+    assert pka.pka_get_device_error() == 0

@@ -368,3 +368,16 @@ def test_decode_rows_on_tensor_cores_plan(cfg):
     f = pka.make_params(hq, hk, b.head_dim, b.page_size, b.layout, b.mask_mode,
                         decode_on_tensor_cores=True, kv_dtype="e4m3")
     assert pka.pka_validate(f, b.qo_indptr, b.kv_indptr, b.last_page_len) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("qo,kv,last", [([0], [0], []), ([0, 0, 0], [0, 2, 3], [3, 1])])
+def test_empty_batches_plan_to_nothing(qo, kv, last):
+    """An empty batch, and a batch whose requests append no rows, plan to no
+    work and no workspace."""
+    h = pka.pka_plan_create()
+    buf = np.zeros(1 << 16, np.uint8)
+    assert pka.pka_plan(h, _p(), _i32(qo), _i32(kv), _i32(last), None, buf, check=False) == OK
+    info = pka.pka_plan_get_info(h)
+    pka.pka_plan_destroy(h)
+    assert info.nnz_qo == 0 and info.num_decode_items == 0 and info.num_prefill_items == 0
+    assert info.float_ws_bytes == 0 and info.num_merge_tasks == 0

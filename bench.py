@@ -152,12 +152,28 @@ def time_steps(fn, steps, warmup, stream, l2_buf=None):
 # Workloads
 # ---------------------------------------------------------------------------
 
+def bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """bf16 bit patterns (uint16) as a bf16 device tensor."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def i32(a, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def kv_tensor(pool: np.ndarray, device="cuda") -> torch.Tensor:
+    """A K/V pool on the device: bf16 from bit patterns, or uint8 e4m3 codes."""
+    if pool.dtype == np.uint8:
+        return torch.from_numpy(np.ascontiguousarray(pool)).to(device)
+    return bf16(pool, device)
+
+
 def decode_setup(device, kv_dtype="bf16", on_tensor_cores=False):
     """Batch-decode workload; kv_dtype "e4m3" stores K/V as 8-bit codes (one
     scale per pool), halving the K/V bytes per key."""
     import paged_kv_attention_plan_gb300 as pka
     from paged_kv_attention_plan_gb300 import workloads as W
-    from tests.gpu_util import bf16, i32, kv_tensor
 
     b = W.batch_decode(seed=1001, kv_dtype=kv_dtype, k_scale=0.5, v_scale=2.0)
     d = dict(batch=b, q=bf16(b.q, device), k=kv_tensor(b.k_pool, device),
@@ -248,7 +264,6 @@ def prefill_setup(device):
     then causal attention of the new rows against their whole history."""
     import paged_kv_attention_plan_gb300 as pka
     from paged_kv_attention_plan_gb300 import workloads as W
-    from tests.gpu_util import bf16, i32
 
     b = W.append_prefill(seed=1002)
     d = dict(batch=b, q=bf16(b.q, device), k=bf16(b.k_pool, device), v=bf16(b.v_pool, device),
@@ -282,7 +297,6 @@ def ragged_setup(device):
     attention over ragged K/V (8 requests, 32/32 heads)."""
     import paged_kv_attention_plan_gb300 as pka
     from paged_kv_attention_plan_gb300 import workloads as W
-    from tests.gpu_util import bf16
 
     b = W.ragged_custom_mask(seed=1004)
     d = dict(batch=b, q=bf16(b.q, device), k=bf16(b.k_pool, device), v=bf16(b.v_pool, device))
@@ -312,7 +326,6 @@ def mixed_setup(device, page_size, layout):
     512 tokens in one plan (decode kernel, tensor-core kernel, merge)."""
     import paged_kv_attention_plan_gb300 as pka
     from paged_kv_attention_plan_gb300 import workloads as W
-    from tests.gpu_util import i32
 
     b = W.mixed_step(seed=1003, page_size=page_size, layout=layout, with_payload=False)
     pool = int(b.extra["pool_pages"])
@@ -348,7 +361,6 @@ def cascade_setup(device):
     page tables each list the prompt's pages."""
     import paged_kv_attention_plan_gb300 as pka
     from paged_kv_attention_plan_gb300 import workloads as W
-    from tests.gpu_util import i32
 
     c = W.shared_prompt_decode(with_payload=False)
     root, own = c.levels

@@ -292,10 +292,12 @@ __device__ __forceinline__ void join_merge(const AttnArgs& a, const PkaDecodeJoi
 
 // Issue the bulk copies of keys [a0, a0 + n) of item w (K and V) into a stage
 // (ES bytes per element).
+// `page` is the page id of key a0 + (lane & 15), loaded ahead by the caller
+// (unused for ragged K/V and for head-major pages).
 template <int D, int ES>
 __device__ __forceinline__ void issue_tile_copies(const AttnArgs& a, const PkaWorkItem& w,
                                                   int a0, int n, int hpc, uint32_t dK,
-                                                  uint32_t dV, uint32_t bar, int lane) {
+                                                  uint32_t dV, uint32_t bar, int lane, int page) {
   const int Hk = a.num_kv_heads;
   const int P = a.page_size;
   const int RS = row_bytes(hpc, D, ES);
@@ -312,7 +314,6 @@ __device__ __forceinline__ void issue_tile_copies(const AttnArgs& a, const PkaWo
     if (a.kv_ragged) {
       off = (int64_t)(w.kv_base + j) * row;
     } else {
-      const int page = a.kv_indices[w.kv_base + j / P];
       off = (int64_t)page * a.page_stride + (int64_t)(j % P) * row;
     }
     off += (int64_t)w.kv_head0 * D;
@@ -422,11 +423,25 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == n_cons) {
     // ---------------- producer warp ----------------
+    // Row copies of paged K/V: the page ids of a tile are loaded one tile
+    // ahead (lanes t and t + 16 hold the page of key t), so their latency
+    // overlaps the wait for a free stage instead of delaying the copies.  With
+    // one-token pages every key has its own id.  (Boxed staging needs one or
+    // two ids a tile and loads them as it issues: loading them ahead measured
+    // slower there.)
+    const int P = a.page_size;
+    const bool ahead = !boxed && !a.kv_ragged && !(a.layout == PKA_HND && P > 1);
+    auto tile_page = [&](const PkaWorkItem& w, int a0) -> int {
+      const int j = a0 + (lane & 15);
+      return j < w.t1 ? a.kv_indices[w.kv_base + j / P] : 0;
+    };
     uint32_t it = 0;
     for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
       const PkaWorkItem w = a.items[ii];
+      int page = ahead ? tile_page(w, w.t0) : 0;
       for (int a0 = w.t0; a0 < w.t1; a0 += TS, ++it) {
         const int s = it % stages;
+        const int next_page = ahead && a0 + TS < w.t1 ? tile_page(w, a0 + TS) : 0;
         if (!mbar_wait(bars.empty(s), ((it / stages) & 1) ^ 1)) {
           record_timeout(a.err, &abort_flag);
           break;
@@ -445,9 +460,10 @@ __global__ void __launch_bounds__(320, 1)
           if (lane == 0) mbar_arrive_expect_tx(bars.full(s), (uint32_t)(2 * n * hpc * D * ES));
           __syncwarp();
           issue_tile_copies<D, ES>(a, w, a0, n, hpc, smem_u32(sK + s * stage_bytes),
-                                   smem_u32(sV + s * stage_bytes), bars.full(s), lane);
+                                   smem_u32(sV + s * stage_bytes), bars.full(s), lane, page);
         }
         mbar_arrive(bars.full(s));
+        page = next_page;
       }
     }
     // Drain: every issued tile's copies must land before the CTA leaves.

@@ -6,7 +6,7 @@
 // list to the device asynchronously, run a stable kernel per layer) and
 // "Load balancing and split-KV decisions" (partition long key ranges across
 // CTAs, merge their partial states).  The pages give no split threshold; the
-// policy here is ours (see split_decode / split_prefill below).
+// policy here is ours (plan_decode and plan_prefill below).
 #include <algorithm>
 #include <cmath>
 #include <cstddef>
@@ -20,6 +20,46 @@
 
 using pka::AttnArgs;
 
+namespace pka {
+
+// The planner's lists.  A plan object keeps them from one plan to the next:
+// each plan clears them (the capacity stays), so steady-state planning does
+// not allocate, which matters for a cascade's tens of thousands of merge slots.
+struct PlanLists {
+  std::vector<int32_t> dec_cta_ptr{0};
+  std::vector<PkaWorkItem> dec_items;
+  std::vector<int32_t> pre_cta_ptr{0};
+  std::vector<PkaWorkItem> pre_items;
+  std::vector<PkaMergeTask> merges;
+  std::vector<PkaDecodeJoin> joins;  // split decode units, merged in the decode kernel
+  int32_t records = 0;
+  int32_t joined_pairs = 0;  // (row, qo head) pairs the decode kernel merges
+  int32_t decode_chunk = 0;
+  // Cascade: every piece writes partial records and each (row, head) merges
+  // the records of all levels, listed in merge_slots.
+  bool cascade = false;
+  struct Slot { int32_t row, head, rec; };
+  std::vector<Slot> slots;
+  std::vector<int32_t> merge_slots;
+
+  void reset(bool is_cascade) {
+    dec_cta_ptr.assign(1, 0);
+    dec_items.clear();
+    pre_cta_ptr.assign(1, 0);
+    pre_items.clear();
+    merges.clear();
+    joins.clear();
+    records = joined_pairs = decode_chunk = 0;
+    cascade = is_cascade;
+    slots.clear();
+    merge_slots.clear();
+  }
+};
+
+}  // namespace pka
+
+using pka::PlanLists;
+
 struct pka_plan_s {
   pka_params params{};
   bool planned = false;
@@ -31,6 +71,7 @@ struct pka_plan_s {
   int device = -1;
   int32_t layout_records = 0;  // partial records the float workspace is laid out for
   int32_t merge_capacity = 0;  // graph mode: merge tasks the image has room for
+  PlanLists lists;             // the planner's lists, reused by every plan
 };
 
 namespace {
@@ -196,24 +237,6 @@ PkaWorkItem make_item(const Batch& b, int r, int kv_head0, int n_kv_heads, int q
   return it;
 }
 
-struct PlanLists {
-  std::vector<int32_t> dec_cta_ptr{0};
-  std::vector<PkaWorkItem> dec_items;
-  std::vector<int32_t> pre_cta_ptr{0};
-  std::vector<PkaWorkItem> pre_items;
-  std::vector<PkaMergeTask> merges;
-  std::vector<PkaDecodeJoin> joins;  // split decode units, merged in the decode kernel
-  int32_t records = 0;
-  int32_t joined_pairs = 0;  // (row, qo head) pairs the decode kernel merges
-  int32_t decode_chunk = 0;
-  // Cascade: every piece writes partial records and each (row, head) merges
-  // the records of all levels, listed in merge_slots.
-  bool cascade = false;
-  struct Slot { int32_t row, head, rec; };
-  std::vector<Slot> slots;
-  std::vector<int32_t> merge_slots;
-};
-
 // Give the pieces of one split unit their partial records and merge tasks.
 // `pieces` index into `items`; each piece writes q_count * heads records laid
 // out [token][qo head]; the heads are heads_total qo heads starting at head0.
@@ -244,10 +267,14 @@ void assign_records(PlanLists* L, std::vector<PkaWorkItem>& items,
     return;
   }
   if (L->cascade) {
+    // filled through a pointer: a push_back per slot through L measured 5x slower
+    const size_t at = L->slots.size();
+    L->slots.resize(at + pieces.size() * (size_t)per);
+    PlanLists::Slot* o = L->slots.data() + at;
     for (size_t k = 0; k < pieces.size(); ++k)
       for (int i = 0; i < q_count; ++i)
         for (int h = 0; h < heads_total; ++h)
-          L->slots.push_back({q_row0 + i, head0 + h, base + (int)k * per + i * heads_total + h});
+          *o++ = {q_row0 + i, head0 + h, base + (int)k * per + i * heads_total + h};
     return;
   }
   for (int i = 0; i < q_count; ++i)
@@ -266,21 +293,33 @@ void assign_records(PlanLists* L, std::vector<PkaWorkItem>& items,
 // listed contiguously in merge_slots (a counting sort by row and head).
 void build_slot_merges(PlanLists* L, int32_t nnz, int32_t heads) {
   const int64_t keys = (int64_t)nnz * heads;
+  const size_t n = L->slots.size();
+  const PlanLists::Slot* sl = L->slots.data();
   std::vector<int32_t> start(keys + 1, 0);
-  for (const auto& s : L->slots) ++start[(int64_t)s.row * heads + s.head + 1];
-  for (int64_t k = 0; k < keys; ++k) start[k + 1] += start[k];
-  L->merge_slots.assign(L->slots.size(), 0);
-  std::vector<int32_t> pos(start.begin(), start.end() - 1);
-  for (const auto& s : L->slots) L->merge_slots[pos[(int64_t)s.row * heads + s.head]++] = s.rec;
+  int32_t* st = start.data();
+  for (size_t i = 0; i < n; ++i) ++st[(int64_t)sl[i].row * heads + sl[i].head + 1];
+  int64_t used = 0;  // (row, head) pairs with at least one record
   for (int64_t k = 0; k < keys; ++k) {
-    if (start[k + 1] == start[k]) continue;
-    PkaMergeTask t{};
-    t.out_row = (int32_t)(k / heads);
-    t.head = (int32_t)(k % heads);
-    t.rec_first = start[k];
-    t.nslots = start[k + 1] - start[k];
-    t.rec_stride = 0;  // list mode
-    L->merges.push_back(t);
+    used += st[k + 1] > 0;
+    st[k + 1] += st[k];
+  }
+  L->merge_slots.resize(n);
+  int32_t* out = L->merge_slots.data();
+  std::vector<int32_t> pos(start.begin(), start.end() - 1);
+  int32_t* ps = pos.data();
+  for (size_t i = 0; i < n; ++i) out[ps[(int64_t)sl[i].row * heads + sl[i].head]++] = sl[i].rec;
+  const size_t m0 = L->merges.size();
+  L->merges.resize(m0 + (size_t)used);
+  PkaMergeTask* t = L->merges.data() + m0;
+  for (int64_t k = 0; k < keys; ++k) {
+    if (st[k + 1] == st[k]) continue;
+    *t = PkaMergeTask{};
+    t->out_row = (int32_t)(k / heads);
+    t->head = (int32_t)(k % heads);
+    t->rec_first = st[k];
+    t->nslots = st[k + 1] - st[k];
+    t->rec_stride = 0;  // list mode
+    ++t;
   }
 }
 
@@ -563,8 +602,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
     return PKA_ERR_WORKSPACE;
   }
 
-  PlanLists L;
-  L.cascade = cascade;
+  PlanLists& L = plan->lists;
+  L.reset(cascade);
   plan_decode(p, lv, num_sms, &L);
   plan_prefill(p, lv, num_sms, &L);
   if (cascade) build_slot_merges(&L, nnz, p->num_qo_heads);

@@ -274,6 +274,52 @@ def test_plan_is_deterministic():
     assert np.array_equal(a, c)
 
 
+def test_replanning_one_handle_matches_fresh_handles():
+    """A plan object reuses its planner lists from plan to plan: a sequence of
+    different batches and cascades planned on one handle gives, byte for byte,
+    the images that a fresh handle gives for each."""
+    c = W.make_cascade_batch(31, [1, 1, 5, 1, 40], [300, 17, 900, 64, 1200],
+                             [[(5, 2000)], [(2, 160), (3, 0)]], page_size=4, with_payload=False)
+    levels = [(lv["qo_indptr"], lv["kv_indptr"], lv["last_page_len"]) for lv in c.levels]
+    dec = W.batch_decode(with_payload=False)
+    mix = W.mixed_step(page_size=16, layout="HND", with_payload=False)
+    runs = [
+        ("cascade", pka.make_params(32, 8, 128, 4, num_sms=152), levels),
+        ("plan", pka.make_params(32, 8, 128, 16, num_sms=152),
+         (None, dec.kv_indptr, dec.last_page_len)),
+        ("plan", pka.make_params(32, 8, 128, 16, "HND", split_mode="fixed", fixed_split_pages=5,
+                                 num_sms=152), (mix.qo_indptr, mix.kv_indptr, mix.last_page_len)),
+        ("cascade", pka.make_params(32, 8, 128, 4, mask_mode="none", split_mode="off",
+                                    num_sms=152), levels),
+        ("plan", pka.make_params(32, 8, 128, 16, "HND", num_sms=152, graph_max_batch=200,
+                                 graph_max_qo_rows=4096),
+         (mix.qo_indptr, mix.kv_indptr, mix.last_page_len)),
+    ]
+
+    def image(h, kind, params, args):
+        buf = np.zeros(1 << 24, np.uint8)
+        if kind == "cascade":
+            s = pka.pka_plan_cascade(h, params, args, None, buf, check=False)
+        else:
+            s = pka.pka_plan(h, params, *args, None, buf, check=False)
+        assert s == 0
+        return buf[:int(pka.pka_plan_get_info(h).int_ws_bytes)].copy()
+
+    fresh = []
+    for r in runs:
+        h = pka.pka_plan_create()
+        try:
+            fresh.append(image(h, *r))
+        finally:
+            pka.pka_plan_destroy(h)
+    h = pka.pka_plan_create()
+    try:
+        for r, want in zip(runs + runs[::-1], fresh + fresh[::-1]):
+            assert np.array_equal(image(h, *r), want)
+    finally:
+        pka.pka_plan_destroy(h)
+
+
 def test_workspace_too_small_reports_sizes():
     h = pka.pka_plan_create()
     try:

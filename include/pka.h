@@ -29,9 +29,12 @@
  *   - Payloads (q, k, v, o, k_new, v_new) are bfloat16; lse is float32 in
  *     base-2 units; index arrays are int32.
  *   - "_h" pointers are host memory, "_d" and payload pointers device memory.
- *   - The library allocates no device or host memory.  The caller owns every
- *     buffer; pka_plan_create allocates the small host plan object (and one
- *     CUDA event on the first pka_plan with a device workspace).
+ *   - The library allocates no device memory and no pinned memory.  The
+ *     caller owns every buffer; pka_plan_create allocates the host plan
+ *     object (and one CUDA event on the first pka_plan with a device
+ *     workspace).  The plan object keeps the planner's host work lists from
+ *     one plan to the next (their size follows the largest plan so far)
+ *     until pka_plan_destroy, so steady-state planning does not allocate.
  *   - All device work is ordered on the caller's stream, passed as a
  *     cudaStream_t cast to void* (NULL = legacy default stream).
  *   - Every call returns a pka_status; nothing throws across the ABI and no

@@ -254,13 +254,13 @@ void assign_records(PlanLists* L, std::vector<PkaWorkItem>& items,
   if (join_kv_heads > 0 && !L->cascade) {
     const int g = heads_total / join_kv_heads;
     const int j0 = (int)L->joins.size();
+    L->joins.resize((size_t)j0 + join_kv_heads);
+    PkaDecodeJoin* jo = L->joins.data() + j0;
     for (int hl = 0; hl < join_kv_heads; ++hl) {
-      PkaDecodeJoin j{};
-      j.arrived = 0;
-      j.rec_first = base + hl * g;
-      j.nslots = (int)pieces.size();
-      j.rec_stride = per;
-      L->joins.push_back(j);
+      jo[hl] = PkaDecodeJoin{};
+      jo[hl].rec_first = base + hl * g;
+      jo[hl].nslots = (int)pieces.size();
+      jo[hl].rec_stride = per;
     }
     for (int k : pieces) items[k].join = j0;
     L->joined_pairs += q_count * heads_total;

@@ -361,6 +361,28 @@ def test_null_arguments_rejected():
                                          None, None, None, 64, None) == INVALID
 
 
+def test_append_rejects_misaligned_buffers_and_strides():
+    """pka_append_paged_kv_cache moves 16-byte row pieces: buffers that are not
+    16-byte aligned, or a page stride that is not whole 16-byte units, are
+    refused before any device work (the pointers below are never read)."""
+    import ctypes
+    lib = _pka.lib()
+    A = 1 << 20  # a 16-byte-aligned stand-in address
+
+    def call(params, k_new=A, v_new=A, k=A, v=A, stride=1024, nnz=5):
+        return lib.pka_append_paged_kv_cache(ctypes.byref(params), 3, k_new, v_new, A, nnz, A, A,
+                                             A, k, v, stride, None)
+
+    bf = _p()
+    for bad in (dict(k_new=A + 8), dict(v_new=A + 2), dict(k=A + 4), dict(v=A + 1),
+                dict(stride=1024 + 4), dict(stride=0), dict(stride=-16)):
+        assert call(bf, **bad) == INVALID, bad
+    f8 = _p(kv_dtype="e4m3")
+    assert call(f8, stride=1024 + 8) == INVALID  # e4m3 rows: 16 elements per 16 bytes
+    assert call(_p(kv_ragged=True)) == UNSUPPORTED
+    assert call(bf, nnz=0) == OK  # nothing to append: no device work
+
+
 def test_fp8_kv_is_decode_only():
     """e4m3 K/V pools are read by the decode kernel only: batches with rows of
     qo_len >= 2 are refused."""

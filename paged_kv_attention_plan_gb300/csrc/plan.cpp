@@ -12,8 +12,6 @@
 #include <cstddef>
 #include <cstdio>
 #include <cstring>
-#include <functional>
-#include <queue>
 #include <vector>
 
 #include "pka_internal.h"
@@ -455,6 +453,32 @@ void plan_decode(const pka_params* p, const std::vector<Batch>& lv, int num_sms,
   order_split_pieces(L);
 }
 
+// Greedy dealing (longest first onto the least loaded CTA): for each index in
+// `order`, the CTA with the smallest (load, CTA id) takes it.  A min-heap of
+// (load, id) pairs with one sift-down per deal (the pairs are distinct, so the
+// choice is the same as with any priority queue).  Fills cta_of.
+void deal_least_loaded(const std::vector<int>& order, const std::vector<int64_t>& cost, int ctas,
+                       std::vector<int>& cta_of) {
+  using Slot = std::pair<int64_t, int>;
+  std::vector<Slot> hp(ctas);
+  for (int c = 0; c < ctas; ++c) hp[c] = {0, c};  // ascending ids: already a min-heap
+  const size_t m = hp.size();
+  for (int i : order) {
+    const Slot v{hp[0].first + cost[i], hp[0].second};
+    cta_of[i] = hp[0].second;
+    size_t k = 0;
+    for (;;) {
+      size_t c = 2 * k + 1;
+      if (c >= m) break;
+      if (c + 1 < m && hp[c + 1] < hp[c]) ++c;
+      if (!(hp[c] < v)) break;
+      hp[k] = hp[c];
+      k = c;
+    }
+    hp[k] = v;
+  }
+}
+
 // Rows of requests with qo_len >= 2 go to the tensor-core kernel: units are
 // (request, kv head, 2 x 128 / g query tokens): the g qo heads of one kv head
 // pack with the tokens into two 128-row tiles that share every K/V load.  Causal
@@ -493,8 +517,11 @@ void plan_prefill(const pka_params* p, const std::vector<Batch>& lv, int num_sms
   }
   auto& items = L->pre_items;
   std::vector<int64_t> cost;
+  cost.reserve(units.size());
+  items.reserve(units.size());
+  std::vector<int> pieces;  // items of the current unit (reused)
   for (const Unit& u : units) {
-    std::vector<int> pieces;
+    pieces.clear();
     int64_t step = chunk > 0 ? chunk : std::max(u.kend, 1);
     int64_t t = 0;
     do {
@@ -511,22 +538,16 @@ void plan_prefill(const pka_params* p, const std::vector<Batch>& lv, int num_sms
   std::vector<int> order(n);
   for (int i = 0; i < n; ++i) order[i] = i;
   std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return cost[a] > cost[c]; });
-  using Slot = std::pair<int64_t, int>;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int c = 0; c < ctas; ++c) heap.push({0, c});
-  std::vector<std::vector<int>> per(ctas);
-  for (int i : order) {
-    Slot s = heap.top();
-    heap.pop();
-    per[s.second].push_back(i);
-    heap.push({s.first + cost[i], s.second});
-  }
-  std::vector<PkaWorkItem> sorted;
-  sorted.reserve(n);
-  for (int c = 0; c < ctas; ++c) {
-    for (int i : per[c]) sorted.push_back(items[i]);
-    L->pre_cta_ptr.push_back((int)sorted.size());
-  }
+  // The CTA of each item; then the items grouped by CTA, each CTA's in
+  // dealing order (a counting sort).
+  std::vector<int> cta_of(n), start(ctas + 1, 0);
+  deal_least_loaded(order, cost, ctas, cta_of);
+  for (int i = 0; i < n; ++i) ++start[cta_of[i] + 1];
+  for (int c = 0; c < ctas; ++c) start[c + 1] += start[c];
+  std::vector<PkaWorkItem> sorted(n);
+  std::vector<int> pos(start.begin(), start.end() - 1);
+  for (int i : order) sorted[pos[cta_of[i]]++] = items[i];
+  for (int c = 0; c < ctas; ++c) L->pre_cta_ptr.push_back(start[c + 1]);
   items.swap(sorted);
 }
 
@@ -544,16 +565,10 @@ void fold_ctas(std::vector<int32_t>& cta_ptr, std::vector<PkaWorkItem>& items, i
   std::vector<int> order(n);
   for (int c = 0; c < n; ++c) order[c] = c;
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return cost[x] > cost[y]; });
-  using Slot = std::pair<int64_t, int>;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int c = 0; c < ctas; ++c) heap.push({0, c});
+  std::vector<int> cta_of(n);
+  deal_least_loaded(order, cost, ctas, cta_of);
   std::vector<std::vector<int>> per(ctas);
-  for (int c : order) {
-    Slot s = heap.top();
-    heap.pop();
-    per[s.second].push_back(c);
-    heap.push({s.first + cost[c], s.second});
-  }
+  for (int c : order) per[cta_of[c]].push_back(c);
   std::vector<PkaWorkItem> sorted;
   sorted.reserve(items.size());
   std::vector<int32_t> ptr{0};

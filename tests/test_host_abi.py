@@ -266,6 +266,28 @@ def test_auto_split_balances_decode_keys():
     assert sum(loads) == int(np.sum(b.kv_lens))
 
 
+@pytest.mark.parametrize("cfg", ["prefill", "ragged"])
+def test_prefill_deal_is_list_scheduling(cfg):
+    """Tensor-core items are dealt longest first, each to the least loaded CTA
+    (cost = keys + 64): every CTA's load then stays within the mean load plus
+    the largest item, and the per-CTA loads are as even as that greedy rule
+    makes them (no CTA is idle while another holds two or more items)."""
+    b = CONFIGS[cfg]()
+    params = pka.make_params(b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.layout,
+                             b.mask_mode, kv_ragged=b.kv_ragged, num_sms=152)
+    plan, _, _ = _dry_plan(params, b.qo_indptr, b.kv_indptr, b.last_page_len)
+    ptr, items = plan["prefill_cta_ptr"], plan["prefill_items"]
+    cost = [i["t1"] - i["t0"] + 64 for i in items]
+    loads = [sum(cost[ptr[c]:ptr[c + 1]]) for c in range(len(ptr) - 1)]
+    assert len(loads) == min(152, len(items))
+    assert min(ptr[c + 1] - ptr[c] for c in range(len(ptr) - 1)) >= 1
+    assert max(loads) <= sum(loads) / len(loads) + max(cost)
+    # inside a CTA the items come in dealing order: longest first
+    for c in range(len(ptr) - 1):
+        cs = cost[ptr[c]:ptr[c + 1]]
+        assert cs == sorted(cs, reverse=True)
+
+
 def test_plan_is_deterministic():
     b = W.mixed_step(page_size=16, layout="HND", with_payload=False)
     params = pka.make_params(32, 8, 128, 16, "HND", num_sms=152)

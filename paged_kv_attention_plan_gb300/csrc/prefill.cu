@@ -17,7 +17,7 @@
 // of two 128-row query tiles of the same (request, kv head) (thread = row =
 // TMEM lane); warp 8 loads Q and the K ring, warp 10 the V ring (TMA for
 // whole pages, cp.async for the rest), warp 9 allocates TMEM and issues the
-// MMAs.  Both query tiles share each K/V tile and the tensor core alternates
+// MMAs (the whole warp runs the issue loop; one elected lane issues).  Both query tiles share each K/V tile and the tensor core alternates
 // between them, so one tile's MMAs overlap the other tile's softmax.  P stays in tensor memory (it overwrites the first
 // half of its S tile) and feeds the P V product as the A operand.
 #include <cudaTypedefs.h>
@@ -354,13 +354,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::prefetch_tmap(map);
     }
     uint32_t it = 0, q_uses = 0;
-    for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
+    for (int ii = i0; ii < i1 && !warp_any(&abort_flag); ++ii) {
       const PkaWorkItem w = a.items[ii];
       const int n = num_tiles(w);
       if (n == 0) continue;
       if (kq) {
         const bool two = w.q_count > TQ;
-        if (q_uses > 0 && !mbar_wait(smem_u32(&bars.q_empty), (q_uses - 1) & 1)) {
+        if (q_uses > 0 && !mbar_wait_warp(smem_u32(&bars.q_empty), (q_uses - 1) & 1)) {
           fail(a, &abort_flag);
           break;
         }
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int k = 0; k < n; ++k, ++it) {
         const int s = it % ns;
-        if (it >= (uint32_t)ns && !mbar_wait(smem_u32(&empty[s]), ((it / ns) - 1) & 1)) {
+        if (it >= (uint32_t)ns && !mbar_wait_warp(smem_u32(&empty[s]), ((it / ns) - 1) & 1)) {
           fail(a, &abort_flag);
           break;
         }
@@ -399,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Drain: the loads of the last stages must land before the CTA leaves.
     for (uint32_t k = it > (uint32_t)ns ? it - ns : 0; k < it; ++k)
-      if (!mbar_wait(smem_u32(&full[k % ns]), (k / ns) & 1)) fail(a, &abort_flag);
-    if (kq && q_uses > 0 && !mbar_wait(smem_u32(&bars.q_full), (q_uses - 1) & 1))
+      if (!mbar_wait_warp(smem_u32(&full[k % ns]), (k / ns) & 1)) fail(a, &abort_flag);
+    if (kq && q_uses > 0 && !mbar_wait_warp(smem_u32(&bars.q_full), (q_uses - 1) & 1))
       fail(a, &abort_flag);
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -409,7 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so that the tensor core works on one tile while the other tile's
     // softmax runs.  MMAs of one thread execute in issue order, so S_x(k+1)
     // may overwrite the P_x(k) that PV_x(k) reads.
-    if (lane == 0) {
+    // The whole warp runs the loop and every value in it is warp-uniform;
+    // elect.sync inside each MMA and commit picks the one issuing lane.  (The
+    // same loop run by lane 0 alone under a branch issued the MMAs about 20%
+    // slower on the append-prefill workload.)
+    {
       constexpr uint32_t idS = tc::idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(BM, D, false, true);
       uint32_t kv_it = 0, q_uses = 0;
@@ -427,54 +431,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)(((kk / 4) * BLK + (kk % 4) * 32) >> 4);
-          tc::mma_bf16(d, ad + off, bd + off, idS, kk > 0 ? 1u : 0u);
+          tc::mma_bf16_elect(d, ad + off, bd + off, idS, kk > 0 ? 1u : 0u);
         }
-        tc::mma_commit(smem_u32(&bars.s_full[x]));
+        tc::mma_commit_elect(smem_u32(&bars.s_full[x]));
       };
       auto issue_pv = [&](int x, uint32_t it, bool first) {
         const uint64_t bd = dv0 + (uint64_t)(((it % VS) * NB * BLK) >> 4);
         const uint32_t d = tmem + 256 + x * 128, pa = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          tc::mma_bf16_ts(d, pa + kk * 8, bd + (uint64_t)((kk * 2048) >> 4), idO,
-                          (first && kk == 0) ? 0u : 1u);
-        tc::mma_commit(smem_u32(&bars.o_done[x]));
+          tc::mma_bf16_ts_elect(d, pa + kk * 8, bd + (uint64_t)((kk * 2048) >> 4), idO,
+                                (first && kk == 0) ? 0u : 1u);
+        tc::mma_commit_elect(smem_u32(&bars.o_done[x]));
       };
-      for (int ii = i0; ii < i1 && ok && !abort_flag; ++ii) {
+      for (int ii = i0; ii < i1 && ok && !warp_any(&abort_flag); ++ii) {
         const PkaWorkItem w = a.items[ii];
         const int n = num_tiles(w);
         if (n == 0) continue;
         const int nx = w.q_count > TQ ? 2 : 1;
-        ok = mbar_wait(smem_u32(&bars.q_full), q_uses & 1);
+        ok = mbar_wait_warp(smem_u32(&bars.q_full), q_uses & 1);
         ++q_uses;
-        if (ok) ok = mbar_wait(smem_u32(&bars.k_full[kv_it % KS]), (kv_it / KS) & 1);
+        if (ok) ok = mbar_wait_warp(smem_u32(&bars.k_full[kv_it % KS]), (kv_it / KS) & 1);
         if (!ok) break;
         tc::fence_after_sync();
         for (int x = 0; x < nx; ++x) issue_s(x, kv_it);
-        tc::mma_commit(smem_u32(&bars.k_empty[kv_it % KS]));
+        tc::mma_commit_elect(smem_u32(&bars.k_empty[kv_it % KS]));
         for (int k = 0; k < n && ok; ++k) {
           const uint32_t it = kv_it + k;
           for (int x = 0; x < nx && ok; ++x) {
             const uint32_t ux = x ? uses1 : uses0, ox = x ? o_uses1 : o_uses0;
-            ok = mbar_wait(smem_u32(&bars.p_full[x]), (ux + k) & 1);
-            if (ok && k == 0 && ox > 0) ok = mbar_wait(smem_u32(&bars.o_free[x]), (ox - 1) & 1);
-            if (ok && x == 0) ok = mbar_wait(smem_u32(&bars.v_full[it % VS]), (it / VS) & 1);
+            ok = mbar_wait_warp(smem_u32(&bars.p_full[x]), (ux + k) & 1);
+            if (ok && k == 0 && ox > 0)
+              ok = mbar_wait_warp(smem_u32(&bars.o_free[x]), (ox - 1) & 1);
+            if (ok && x == 0) ok = mbar_wait_warp(smem_u32(&bars.v_full[it % VS]), (it / VS) & 1);
             if (!ok) break;
             tc::fence_after_sync();
             issue_pv(x, it, k == 0);
             if (k + 1 < n) {
               if (x == 0) {
-                ok = mbar_wait(smem_u32(&bars.k_full[(it + 1) % KS]), ((it + 1) / KS) & 1);
+                ok = mbar_wait_warp(smem_u32(&bars.k_full[(it + 1) % KS]), ((it + 1) / KS) & 1);
                 if (!ok) break;
                 tc::fence_after_sync();
               }
               issue_s(x, it + 1);
-              if (x == nx - 1) tc::mma_commit(smem_u32(&bars.k_empty[(it + 1) % KS]));
+              if (x == nx - 1) tc::mma_commit_elect(smem_u32(&bars.k_empty[(it + 1) % KS]));
             }
           }
-          tc::mma_commit(smem_u32(&bars.v_empty[it % VS]));
+          tc::mma_commit_elect(smem_u32(&bars.v_empty[it % VS]));
         }
-        tc::mma_commit(smem_u32(&bars.q_empty));
+        tc::mma_commit_elect(smem_u32(&bars.q_empty));
         uses0 += n;
         o_uses0 += 1;
         if (nx == 2) {
@@ -485,7 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) fail(a, &abort_flag);
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int x = warp >> 2;                 // query tile of this warpgroup
@@ -496,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_tok = x * TQ + row / G, g = row % G;
     const float sc = a.scale_log2;
     uint32_t uses = 0;
-    for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
+    for (int ii = i0; ii < i1 && !warp_any(&abort_flag); ++ii) {
       const PkaWorkItem w = a.items[ii];
       if (x == 1 && w.q_count <= TQ) continue;  // no second tile in this item
       const int n = num_tiles(w);
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
         if (mm == PKA_MASK_CUSTOM)
           load_mask_bits(a.mask, mrow + kb, mrow + min(w.t1, w.kv_len), mbits);
-        if (!mbar_wait(smem_u32(&bars.s_full[x]), (uses + k) & 1)) {
+        if (!mbar_wait_warp(smem_u32(&bars.s_full[x]), (uses + k) & 1)) {
           ok = false;
           break;
         }
@@ -568,6 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // probabilities (masked scores are -inf and give 0) -> P, bf16, packed
         // in place over the consumed scores and stored over the first 64
         // columns of S
+        // With m = -inf every score of the row so far is -inf (masked), and
+        // -inf * scale + 0 = -inf gives p = ex2(-inf) = 0 with no select (the
+        // scale is positive).
         float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         const bool none = m == -INFINITY;
         const float neg_m = none ? 0.f : -m;
@@ -578,9 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; j += 2) {
             const float2 t2 = __ffma2_rn(
                 make_float2(__uint_as_float(r[c][j]), __uint_as_float(r[c][j + 1])), sc2, negm2);
-            float p0 = ex2(t2.x);
-            float p1 = ex2(t2.y);
-            if (none) p0 = p1 = 0.f;
+            const float p0 = ex2(t2.x);
+            const float p1 = ex2(t2.y);
             sum2[(j >> 1) & 1] = __fadd2_rn(sum2[(j >> 1) & 1], make_float2(p0, p1));
             r[c][j / 2] = float2_to_bf16x2(p0, p1);
           }
@@ -617,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rec = w.out_rec + i_tok * G + g;
       float* pdst = a.part_o + (int64_t)rec * D;
       if (n > 0) {
-        if (!mbar_wait(smem_u32(&bars.o_done[x]), (uses + n - 1) & 1)) {
+        if (!mbar_wait_warp(smem_u32(&bars.o_done[x]), (uses + n - 1) & 1)) {
           fail(a, &abort_flag);
           break;
         }
@@ -744,27 +750,25 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Encode the launch's tensor maps; returns whether the row maps for gather4
+// were made (0 / 1), or -1 on failure.
 template <int D>
-cudaError_t launch_t(PrefillParams pp, int num_ctas, int nnz_q, int64_t total_kv,
-                     cudaStream_t stream) {
-  const AttnArgs& a = pp.a;
+int encode_maps(Maps& maps, const AttnArgs& a, int G, int nnz_q, int64_t total_kv) {
   int pp_gather = 0;
-  const int G = pp.group;
   const uint64_t Hq = a.num_qo_heads, Hk = a.num_kv_heads;
-  Maps maps;
   std::memset(&maps, 0, sizeof(maps));
   {
     const uint64_t dims[3] = {(uint64_t)D, Hq, (uint64_t)(nnz_q > 0 ? nnz_q : 1)};
     const uint64_t str[2] = {(uint64_t)D * 2, Hq * D * 2};
     const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)(BM / G)};
-    if (!encode(&maps.q, a.q, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode(&maps.q, a.q, 3, dims, str, box)) return -1;
   }
   if (a.kv_ragged) {
     const uint64_t dims[3] = {(uint64_t)D, Hk, (uint64_t)(total_kv > 0 ? total_kv : 1)};
     const uint64_t str[2] = {(uint64_t)D * 2, Hk * D * 2};
     const uint32_t box[3] = {64, 1, (uint32_t)BN};
     if (!encode(&maps.kv_k, a.k, 3, dims, str, box) || !encode(&maps.kv_v, a.v, 3, dims, str, box))
-      return cudaErrorInvalidValue;
+      return -1;
   } else {
     // One box = one whole page of one kv head.  Pages of other sizes, and
     // partial pages, are gathered with cp.async and never use the map.
@@ -783,7 +787,7 @@ cudaError_t launch_t(PrefillParams pp, int num_ctas, int nnz_q, int64_t total_kv
       box[0] = 64; box[1] = pb; box[2] = 1; box[3] = 1;
     }
     if (!encode(&maps.kv_k, a.k, 4, dims, str, box) || !encode(&maps.kv_v, a.v, 4, dims, str, box))
-      return cudaErrorInvalidValue;
+      return -1;
     // The pool as rows of D elements (one kv head of one slot), for gather4:
     // row = page * (page_stride / D) + the slot's and head's row in the page.
     if (a.page_stride % D == 0) {
@@ -792,16 +796,41 @@ cudaError_t launch_t(PrefillParams pp, int num_ctas, int nnz_q, int64_t total_kv
       const uint32_t rbox[2] = {64, 1};
       if (!encode(&maps.row_k, a.k, 2, rdims, rstr, rbox) ||
           !encode(&maps.row_v, a.v, 2, rdims, rstr, rbox))
-        return cudaErrorInvalidValue;
+        return -1;
       pp_gather = 1;
     }
+  }
+  return pp_gather;
+}
+
+template <int D>
+cudaError_t launch_t(PrefillParams pp, int num_ctas, int nnz_q, int64_t total_kv,
+                     MapCache* cache, cudaStream_t stream) {
+  const AttnArgs& a = pp.a;
+  static_assert(sizeof(Maps) <= sizeof(MapCache::maps), "map cache too small");
+  Maps maps;
+  // the maps describe Q and the K/V pools: encode them again only when one of
+  // the buffers, its stride or its declared rows differ from the cached ones
+  const uint64_t key[MapCache::kKeyWords] = {
+      reinterpret_cast<uintptr_t>(a.q), reinterpret_cast<uintptr_t>(a.k),
+      reinterpret_cast<uintptr_t>(a.v), (uint64_t)a.page_stride, (uint64_t)a.page_size,
+      (uint64_t)a.layout, (uint64_t)a.kv_ragged, (uint64_t)a.num_qo_heads,
+      (uint64_t)a.num_kv_heads, (uint64_t)pp.group, (uint64_t)nnz_q, (uint64_t)total_kv,
+      (uint64_t)D, 0, 0, 0};
+  int pp_gather;
+  if (cache && cache->hit(key)) {
+    std::memcpy(&maps, cache->maps, sizeof(maps));
+    pp_gather = cache->aux;
+  } else {
+    pp_gather = encode_maps<D>(maps, a, pp.group, nnz_q, total_kv);
+    if (pp_gather < 0) return cudaErrorInvalidValue;
+    if (cache) cache->store(key, &maps, sizeof(maps), pp_gather);
   }
   constexpr int NB = D / 64;
   // At least 120 KiB, so that one CTA (and its 512 TMEM columns) owns each SM.
   size_t smem = 1024 + (size_t)(2 + Ring<D>::K + Ring<D>::V) * NB * BLK;
   if (smem < 120 * 1024) smem = 120 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem<prefill_kernel<D>>((int)smem);
   if (e != cudaSuccess) return e;
   pp.gather = pp_gather;
   pp.rows_per_page = pp_gather ? a.page_stride / D : 0;
@@ -812,13 +841,13 @@ cudaError_t launch_t(PrefillParams pp, int num_ctas, int nnz_q, int64_t total_kv
 }  // namespace
 
 cudaError_t launch_prefill(const AttnArgs& a0, int num_ctas, int head_dim, int group,
-                           int nnz_q, int64_t total_kv, cudaStream_t stream) {
+                           int nnz_q, int64_t total_kv, MapCache* cache, cudaStream_t stream) {
   PrefillParams pp;
   pp.a = a0;
   pp.a.err = device_error_word();
   pp.group = group;
-  if (head_dim == 128) return launch_t<128>(pp, num_ctas, nnz_q, total_kv, stream);
-  return launch_t<64>(pp, num_ctas, nnz_q, total_kv, stream);
+  if (head_dim == 128) return launch_t<128>(pp, num_ctas, nnz_q, total_kv, cache, stream);
+  return launch_t<64>(pp, num_ctas, nnz_q, total_kv, cache, stream);
 }
 
 }  // namespace pka

@@ -316,6 +316,45 @@ const char* pka_last_error(void);
  * barrier (0 = none, else a pka_status).  Synchronises `stream`. */
 pka_status pka_get_device_error(int32_t* code, void* stream);
 
+/* Host check of a page table ("Deep Dive - FlashInfer", "Where FlashInfer
+ * sits in a serving stack": pages reused while another request still reads
+ * them, and page tables that disagree with last_page_len, are the bugs of
+ * the allocator boundary).  The kernels read kv_indices as given and do not
+ * bound-check page ids, so a caller that cannot vouch for its page table
+ * calls this first.  Host memory only; no CUDA call.
+ *   Checks the length contract (as pka_validate), that kv_indptr_h[batch] <=
+ *   num_indices, and that every page id kv_indices_h[kv_indptr_h[r] ..
+ *   kv_indptr_h[r+1]) lies in [0, num_pool_pages).  With append_indptr_h
+ *   (the rows each request appends this step, as pka_append_paged_kv_cache
+ *   takes them; NULL: no appends), it also checks that no (page, slot) that
+ *   one request appends to is appended to by another request, or lies in
+ *   another request's history (its first kv_len - append_len positions).
+ *   Pages that several requests only read (a shared prefix) are allowed.
+ *   Returns PKA_ERR_METADATA on the first violation, with *bad_index (may be
+ *   NULL) set to the position in kv_indices_h of the offending page id (-1
+ *   for a length-contract violation); PKA_ERR_INVALID_ARG for null arrays or
+ *   a short kv_indices_h; PKA_ERR_UNSUPPORTED for ragged K/V. */
+pka_status pka_check_indices(const pka_params* params, int32_t batch,
+                             const int32_t* append_indptr_h, const int32_t* kv_indptr_h,
+                             const int32_t* kv_indices_h, int64_t num_indices,
+                             const int32_t* last_page_len_h, int64_t num_pool_pages,
+                             int64_t* bad_index);
+
+/* Self-test of the bounded barrier waits behind PKA_ERR_DEVICE_TIMEOUT
+ * (failure detection; the pages have no counterpart).  Launches one small
+ * kernel whose waits use the same code as the attention kernels: two warps
+ * wait together (a warp-wide decision, so a timeout never splits a warp) and
+ * one thread waits alone, on a barrier with `polls` polls of at most 1 ms
+ * each (1 <= polls <= 1000).
+ *   arrive == 0: nothing arrives on the barrier; every wait gives up and the
+ *     kernel records PKA_ERR_DEVICE_TIMEOUT in the device error word (read
+ *     and clear it with pka_get_device_error), then returns normally.
+ *   arrive == 1: one thread arrives first; no wait runs out and nothing is
+ *     recorded.
+ * Either way the kernel ends by itself and the CUDA context stays usable.
+ * PKA_ERR_INVALID_ARG for other arrive or polls values. */
+pka_status pka_selftest_bounded_wait(int32_t arrive, int32_t polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,8 @@ from ._pka import (PKA_HND, PKA_KV_BF16, PKA_KV_FP8_E4M3, PKA_MASK_CAUSAL,  # no
                    pka_append_paged_kv_cache, pka_get_device_error, pka_last_error, pka_merge_states,
                    pka_packbits, pka_plan, pka_plan_cascade, pka_plan_create, pka_plan_destroy,
                    pka_plan_get_info,
-                   pka_plan_wait, pka_run, pka_run_static_scratch, pka_status_str, pka_validate, pka_version)
+                   pka_plan_wait, pka_run, pka_run_static_scratch, pka_status_str, pka_validate, pka_version,
+                   pka_check_indices, pka_selftest_bounded_wait)
 
 __all__ = ["BatchAttention", "make_params", "PkaError"] + [n for n in _pka.EXPORTED]
 

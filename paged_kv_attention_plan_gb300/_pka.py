@@ -29,7 +29,7 @@ EXPORTED = ["pka_status_str", "pka_version", "pka_validate", "pka_plan_create",
             "pka_plan_destroy", "pka_plan", "pka_plan_get_info", "pka_plan_wait", "pka_run",
             "pka_append_paged_kv_cache", "pka_merge_states", "pka_packbits",
             "pka_get_device_error", "pka_last_error", "pka_run_static_scratch",
-            "pka_plan_cascade"]
+            "pka_plan_cascade", "pka_selftest_bounded_wait", "pka_check_indices"]
 
 
 class pka_params(ctypes.Structure):
@@ -104,6 +104,8 @@ def lib():
         L.pka_merge_states.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.pka_packbits.argtypes = [vp, i64, vp, vp]
         L.pka_get_device_error.argtypes = [P(i32), vp]
+        L.pka_selftest_bounded_wait.argtypes = [i32, i32, vp]
+        L.pka_check_indices.argtypes = [P(pka_params), i32, vp, vp, vp, i64, vp, i64, P(i64)]
         L.pka_last_error.argtypes = []
         L.pka_last_error.restype = ctypes.c_char_p
         for name in EXPORTED:
@@ -361,3 +363,22 @@ def pka_get_device_error(stream=None) -> int:
     code = ctypes.c_int32()
     _check(lib().pka_get_device_error(ctypes.byref(code), _stream(stream)), "pka_get_device_error")
     return code.value
+
+
+def pka_selftest_bounded_wait(arrive: bool, polls: int, stream=None):
+    _check(lib().pka_selftest_bounded_wait(1 if arrive else 0, int(polls), _stream(stream)),
+           "pka_selftest_bounded_wait")
+
+
+def pka_check_indices(params, kv_indptr, kv_indices, last_page_len, num_pool_pages,
+                      append_indptr=None):
+    """Host check of a page table; returns (status, bad_index) without raising."""
+    kv = _int32_host(kv_indptr, "kv_indptr")
+    idx = _int32_host(kv_indices, "kv_indices")
+    last = _int32_host(last_page_len, "last_page_len")
+    app = _int32_host(append_indptr, "append_indptr")
+    bad = ctypes.c_int64(-2)
+    s = lib().pka_check_indices(ctypes.byref(params), len(kv) - 1, _ptr(app), _ptr(kv),
+                                _ptr(idx), len(idx), _ptr(last), int(num_pool_pages),
+                                ctypes.byref(bad))
+    return s, bad.value

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libpka.so")
-SOURCES = ["plan.cpp", "decode.cu", "prefill.cu", "util.cu", "static_scratch.cu"]
+SOURCES = ["plan.cpp", "check.cpp", "decode.cu", "prefill.cu", "util.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -436,13 +436,13 @@ __global__ void __launch_bounds__(320, 1)
       return j < w.t1 ? a.kv_indices[w.kv_base + j / P] : 0;
     };
     uint32_t it = 0;
-    for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
+    for (int ii = i0; ii < i1 && !warp_any(&abort_flag); ++ii) {
       const PkaWorkItem w = a.items[ii];
       int page = ahead ? tile_page(w, w.t0) : 0;
       for (int a0 = w.t0; a0 < w.t1; a0 += TS, ++it) {
         const int s = it % stages;
         const int next_page = ahead && a0 + TS < w.t1 ? tile_page(w, a0 + TS) : 0;
-        if (!mbar_wait(bars.empty(s), ((it / stages) & 1) ^ 1)) {
+        if (!mbar_wait_warp(bars.empty(s), ((it / stages) & 1) ^ 1)) {
           record_timeout(a.err, &abort_flag);
           break;
         }
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(320, 1)
     // Drain: every issued tile's copies must land before the CTA leaves.
     const uint32_t first = it > (uint32_t)stages ? it - stages : 0;
     for (uint32_t k = first; k < it; ++k)
-      if (!mbar_wait(bars.full(k % stages), (k / stages) & 1)) record_timeout(a.err, &abort_flag);
+      if (!mbar_wait_warp(bars.full(k % stages), (k / stages) & 1)) record_timeout(a.err, &abort_flag);
     return;
   }
   if (warp == n_cons + 1) {
@@ -481,11 +481,11 @@ __global__ void __launch_bounds__(320, 1)
     // the count merge all pieces (rare: such a piece is normally the first
     // item of its CTA, and its unit's other pieces end later).
     uint32_t jc = 0;
-    for (int ii = i0; ii < i1 - 1 && !abort_flag; ++ii) {
+    for (int ii = i0; ii < i1 - 1 && !warp_any(&abort_flag); ++ii) {
       const PkaWorkItem w = a.items[ii];
       if (w.join < 0 || !a.joins) continue;
       const int s = jc % kJoinRing;
-      if (!mbar_wait(smem_u32(&jfull[s]), (jc / kJoinRing) & 1)) {
+      if (!mbar_wait_warp(smem_u32(&jfull[s]), (jc / kJoinRing) & 1)) {
         record_timeout(a.err, &abort_flag);
         break;
       }
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sK0 = smem_u32(sK), sV0 = smem_u32(sV);
   const float sc = a.scale_log2;
   uint32_t it = 0, jc = 0;
-  for (int ii = i0; ii < i1 && !abort_flag; ++ii) {
+  for (int ii = i0; ii < i1 && !warp_any(&abort_flag); ++ii) {
     const PkaWorkItem w = a.items[ii];
     const int head_base = (w.kv_head0 + hl) * G;  // first qo head of this kv head
     // split piece: the join's fixed fields now, the counter during the last tile
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(320, 1)
       const int s = it % stages;
       if (jp && a0 + TS >= w.t1 && lane == 0)
         hint = *reinterpret_cast<volatile int32_t*>(&jp->arrived);
-      if (!mbar_wait(bars.full(s), (it / stages) & 1)) {
+      if (!mbar_wait_warp(bars.full(s), (it / stages) & 1)) {
         record_timeout(a.err, &abort_flag);
         break;
       }
@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.empty(s));
     }
-    if (abort_flag) break;
+    if (warp_any(&abort_flag)) break;
 
     // Sum the exp shares over the 8 key groups; normalise and write.
 #pragma unroll
@@ -850,14 +850,29 @@ bool encode_box(CUtensorMap* m, const void* base, const AttnArgs& a, int D, int 
 }
 
 template <int D, bool F8>
-cudaError_t launch_t(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
+cudaError_t launch_t(const AttnArgs& a, int num_ctas, MapCache* cache, cudaStream_t stream) {
   constexpr int ES = F8 ? 1 : 2;
   const int hpc = a.heads_per_cta;
+  static_assert(sizeof(DecodeMaps) <= sizeof(MapCache::maps), "map cache too small");
   DecodeMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   int hb = use_boxes(a.page_size, a.kv_ragged, D, ES) ? box_heads(a.layout, hpc) : 0;
-  if (hb && (!encode_box(&maps.k, a.k, a, D, ES, hb) || !encode_box(&maps.v, a.v, a, D, ES, hb)))
-    hb = 0;  // fall back to one bulk copy per key row
+  if (hb) {
+    // the boxed maps describe the pools: encode them again only when the
+    // pools, their layout or the head block differ from the cached ones
+    const uint64_t key[MapCache::kKeyWords] = {
+        reinterpret_cast<uintptr_t>(a.k), reinterpret_cast<uintptr_t>(a.v),
+        (uint64_t)a.page_stride, (uint64_t)a.page_size, (uint64_t)a.layout,
+        (uint64_t)a.num_kv_heads, (uint64_t)D, (uint64_t)ES, (uint64_t)hb, 0, 0, 0, 0, 0, 0, 0};
+    if (cache && cache->hit(key)) {
+      std::memcpy(&maps, cache->maps, sizeof(maps));
+      hb = cache->aux;
+    } else {
+      if (!encode_box(&maps.k, a.k, a, D, ES, hb) || !encode_box(&maps.v, a.v, a, D, ES, hb))
+        hb = 0;  // fall back to one bulk copy per key row
+      if (cache) cache->store(key, &maps, sizeof(maps), hb);
+    }
+  }
   const int stage_bytes = 2 * (hb ? (D * ES / 128) * TS * hb * 128 : TS * row_bytes(hpc, D, ES));
   const int scratch = F8 ? hpc * TS * vs_row_bytes(D) : 0;
   int stages = (kStageBudget - scratch) / stage_bytes;
@@ -866,8 +881,7 @@ cudaError_t launch_t(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
   // the swizzled blocks need 1024-byte alignment: pad the dynamic allocation
   const size_t smem =
       1024 + (size_t)stages * stage_bytes + scratch + 2 * stages * sizeof(uint64_t);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, F8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem<decode_kernel<D, F8>>((int)smem);
   if (e != cudaSuccess) return e;
   decode_kernel<D, F8><<<num_ctas, 32 * (hpc + 2), smem, stream>>>(maps, a, stages, hb);
   return cudaGetLastError();
@@ -876,15 +890,15 @@ cudaError_t launch_t(const AttnArgs& a, int num_ctas, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_decode(const AttnArgs& a0, int num_ctas, int head_dim, int group,
-                          cudaStream_t stream) {
+                          MapCache* cache, cudaStream_t stream) {
   AttnArgs a = a0;
   a.err = device_error_word();
   (void)group;
   if (a.kv_fp8)
-    return head_dim == 128 ? launch_t<128, true>(a, num_ctas, stream)
-                           : launch_t<64, true>(a, num_ctas, stream);
-  return head_dim == 128 ? launch_t<128, false>(a, num_ctas, stream)
-                         : launch_t<64, false>(a, num_ctas, stream);
+    return head_dim == 128 ? launch_t<128, true>(a, num_ctas, cache, stream)
+                           : launch_t<64, true>(a, num_ctas, cache, stream);
+  return head_dim == 128 ? launch_t<128, false>(a, num_ctas, cache, stream)
+                         : launch_t<64, false>(a, num_ctas, cache, stream);
 }
 
 }  // namespace pka

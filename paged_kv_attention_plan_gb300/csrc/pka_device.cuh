@@ -59,12 +59,35 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// Bounded wait for the completion of the phase with the given parity.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait of one thread for the completion of the phase with the given
+// parity (for waits that a single lane of its warp makes).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint32_t polls = kWaitPolls) {
   if (mbar_try_wait(bar, parity)) return true;
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
+  for (uint32_t i = 0; i < polls; ++i)
     if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
   return false;
+}
+
+// Bounded wait made by a whole warp (all 32 lanes converged).  The warp
+// decides together: it goes on once every lane has seen the phase complete,
+// and gives up, all lanes at once, when the common poll count runs out, so
+// a timeout can never leave some lanes waiting and others gone (which would
+// hang the warp at its next shuffle or __syncwarp).  A completed phase stays
+// complete for its parity until the barrier completes the next one, which
+// needs this warp's own later arrival, so lanes that saw it early keep
+// seeing it.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               uint32_t polls = kWaitPolls) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  for (uint32_t i = 0; i < polls; ++i)
+    if (__all_sync(0xffffffffu, mbar_try_wait_suspend(bar, parity, kSuspendNs))) return true;
+  return false;
+}
+
+// Warp-uniform read of a CTA-wide abort flag (all 32 lanes converged).
+__device__ __forceinline__ bool warp_any(volatile int* flag) {
+  return __any_sync(0xffffffffu, *flag != 0);
 }
 
 // Global -> shared bulk copy completing on an mbarrier (16-byte aligned

@@ -3,6 +3,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <cstring>
+
 #include "pka.h"
 #include "pka_plan_image.h"
 
@@ -51,10 +54,55 @@ struct MergeArgs {
   int32_t head_dim;
 };
 
+// Tensor maps of one attention launch, kept in the plan object between runs:
+// a launch encodes its maps again only when something they describe (a
+// buffer address, a stride, a shape) differs from the cached key.
+struct MapCache {
+  static constexpr int kKeyWords = 16;
+  static constexpr int kMaps = 5;
+  uint64_t key[kKeyWords];
+  int valid;
+  int aux;  // a launch setting derived with the maps
+  alignas(64) unsigned char maps[kMaps * 128];  // CUtensorMap objects (128 bytes each)
+
+  bool hit(const uint64_t (&k)[kKeyWords]) const {
+    if (!valid) return false;
+    for (int i = 0; i < kKeyWords; ++i)
+      if (key[i] != k[i]) return false;
+    return true;
+  }
+  void store(const uint64_t (&k)[kKeyWords], const void* m, size_t bytes, int aux_value) {
+    for (int i = 0; i < kKeyWords; ++i) key[i] = k[i];
+    std::memcpy(maps, m, bytes);
+    aux = aux_value;
+    valid = 1;
+  }
+};
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `Kernel` only when
+// the current device has not yet been given at least `bytes` (a larger limit
+// set earlier covers every smaller launch).
+template <auto Kernel>
+cudaError_t ensure_dynamic_smem(int bytes) {
+  static std::atomic<int> set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < 64;
+  if (tracked && set[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && tracked) {
+    int cur = set[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !set[dev].compare_exchange_weak(cur, bytes, std::memory_order_acq_rel)) {
+    }
+  }
+  return e;
+}
+
 cudaError_t launch_decode(const AttnArgs& a, int num_ctas, int head_dim, int group,
-                          cudaStream_t stream);
+                          MapCache* cache, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnArgs& a, int num_ctas, int head_dim, int group, int nnz_q,
-                           int64_t total_kv, cudaStream_t stream);
+                           int64_t total_kv, MapCache* cache, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_packbits(const uint8_t* in, int64_t n, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_new,
@@ -62,11 +110,18 @@ cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_
                           const int32_t* kv_indptr, const int32_t* kv_indices,
                           const int32_t* last_page_len, void* k, void* v,
                           int64_t page_stride, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int arrive, int polls, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
 // Device address of the error word on the current device (null on failure).
 int32_t* device_error_word();
 // Set the text pka_last_error returns on this thread.
 void set_last_error(const char* msg);
+// Record a failed CUDA call (its error text and code, after `where`) as the
+// text pka_last_error returns on this thread; returns PKA_ERR_CUDA.
+pka_status cuda_failure(cudaError_t e, const char* where);
+// Multiprocessor count of the current device (cached per device; 0 if the
+// query fails).
+int current_device_sms();
 
 // Decode launch geometry shared by the planner and the kernel: a decode CTA
 // covers `heads_per_cta` kv heads (at most 8, one consumer warp each, so that

@@ -70,6 +70,8 @@ struct pka_plan_s {
   int32_t layout_records = 0;  // partial records the float workspace is laid out for
   int32_t merge_capacity = 0;  // graph mode: merge tasks the image has room for
   PlanLists lists;             // the planner's lists, reused by every plan
+  pka::MapCache decode_maps{};   // tensor maps of the last run's launches
+  pka::MapCache prefill_maps{};
 };
 
 namespace {
@@ -589,6 +591,8 @@ void pka::set_last_error(const char* msg) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
 }
 
+pka_status pka::cuda_failure(cudaError_t e, const char* where) { return cuda_fail(e, where); }
+
 namespace {
 
 // Plan the levels (one for a plain batch) into the image and start its copy.
@@ -928,7 +932,7 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
     a.joins = h.off_decode_joins
                   ? reinterpret_cast<PkaDecodeJoin*>(plan->int_ws_d + h.off_decode_joins)
                   : nullptr;
-    cudaError_t e = pka::launch_decode(a, h.num_decode_ctas, p->head_dim, g, st);
+    cudaError_t e = pka::launch_decode(a, h.num_decode_ctas, p->head_dim, g, &plan->decode_maps, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   if (graph || h.num_prefill_items > 0) {
@@ -937,7 +941,8 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
     // the Q (and ragged K/V) tensor maps span the buffers' declared rows
     const int rows = graph ? p->graph_max_qo_rows : plan->info.nnz_qo;
     const int64_t kv_rows = graph ? p->graph_max_kv_tokens : plan->info.total_kv;
-    cudaError_t e = pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g, rows, kv_rows, st);
+    cudaError_t e = pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g, rows, kv_rows,
+                                         &plan->prefill_maps, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   if (graph ? plan->merge_capacity > 0 : h.num_merge_tasks > 0) {
@@ -1016,6 +1021,12 @@ pka_status pka_get_device_error(int32_t* code, void* stream) {
   if (!code) return PKA_ERR_INVALID_ARG;
   cudaError_t e = pka::read_and_clear_device_error(code, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKA_OK : cuda_fail(e, "device error read");
+}
+
+pka_status pka_selftest_bounded_wait(int32_t arrive, int32_t polls, void* stream) {
+  if ((arrive != 0 && arrive != 1) || polls < 1 || polls > 1000) return PKA_ERR_INVALID_ARG;
+  cudaError_t e = pka::launch_wait_selftest(arrive, polls, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKA_OK : cuda_fail(e, "wait self-test launch");
 }
 
 const char* pka_last_error(void) { return g_last_error; }

@@ -63,8 +63,10 @@ extern "C" pka_status pka_run_static_scratch(pka_plan_t plan, const pka_params* 
   cudaError_t e = cudaSuccess;
   void* scratch = pka::static_scratch_address(&e);
   if (!scratch) {
-    pka::set_last_error("pka_run_static_scratch: cudaGetSymbolAddress of the static scratch failed");
-    return PKA_ERR_CUDA;
+    // clear the failed call's error, so that it does not surface later as the
+    // failure of an unrelated launch
+    cudaGetLastError();
+    return pka::cuda_failure(e, "pka_run_static_scratch: device address of the static scratch");
   }
   return pka_run(plan, params, q, k, v, page_stride, kv_indices_d, packed_mask_d, o, lse, scratch,
                  pka::kStaticScratchBytes, stream);

@@ -24,6 +24,20 @@ int32_t* device_error_word() {
   return cache[dev];
 }
 
+int current_device_sms() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream) {
   int32_t* p = device_error_word();
   if (!p) return cudaErrorInvalidDevice;
@@ -221,9 +235,37 @@ __global__ void __launch_bounds__(256) append_kernel(
   }
 }
 
+// Grid of a grid-stride kernel: enough blocks for the work, at most 32 per
+// multiprocessor of the current device.
+// Self-test of the bounded barrier waits: warps 0 and 1 wait with the
+// warp-wide wait, lane 0 of warp 2 with the single-thread wait, all on one
+// mbarrier of count 1 and with `polls` polls.  With `arrive` set, lane 0 of
+// warp 1 arrives first and no wait runs out; otherwise nothing arrives, every
+// wait gives up, and the kernel records PKA_ERR_DEVICE_TIMEOUT as the real
+// kernels do, then returns.
+__global__ void __launch_bounds__(96) wait_selftest_kernel(int arrive, uint32_t polls,
+                                                           int32_t* err) {
+  __shared__ uint64_t bar;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (arrive && threadIdx.x == 32) mbar_arrive(smem_u32(&bar));
+  bool ok = true;
+  if (warp < 2)
+    ok = mbar_wait_warp(smem_u32(&bar), 0, polls);
+  else if (lane == 0)
+    ok = mbar_wait(smem_u32(&bar), 0, polls);
+  if (!ok && err) atomicExch(err, (int32_t)PKA_ERR_DEVICE_TIMEOUT);
+}
+
 int grid_for(int64_t work, int block) {
   int64_t g = (work + block - 1) / block;
-  if (g > 152 * 32) g = 152 * 32;
+  int sms = current_device_sms();
+  const int64_t cap = 32 * (int64_t)(sms > 0 ? sms : 1);
+  if (g > cap) g = cap;
   return (int)(g < 1 ? 1 : g);
 }
 
@@ -237,6 +279,11 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
     merge_kernel<128><<<blocks, 256, 0, stream>>>(a);
   else
     merge_kernel<64><<<blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int arrive, int polls, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 96, 0, stream>>>(arrive, (uint32_t)polls, device_error_word());
   return cudaGetLastError();
 }
 

@@ -173,7 +173,7 @@ def decode_setup(device, kv_dtype="bf16", on_tensor_cores=False):
     """Batch-decode workload; kv_dtype "e4m3" stores K/V as 8-bit codes (one
     scale per pool), halving the K/V bytes per key."""
     import paged_kv_attention_plan_gb300 as pka
-    from paged_kv_attention_plan_gb300 import workloads as W
+    from inputs import workloads as W
 
     b = W.batch_decode(seed=1001, kv_dtype=kv_dtype, k_scale=0.5, v_scale=2.0)
     d = dict(batch=b, q=bf16(b.q, device), k=kv_tensor(b.k_pool, device),
@@ -263,7 +263,7 @@ def prefill_setup(device):
     """Append-prefill workload: append_paged_kv_cache writes the new rows,
     then causal attention of the new rows against their whole history."""
     import paged_kv_attention_plan_gb300 as pka
-    from paged_kv_attention_plan_gb300 import workloads as W
+    from inputs import workloads as W
 
     b = W.append_prefill(seed=1002)
     d = dict(batch=b, q=bf16(b.q, device), k=bf16(b.k_pool, device), v=bf16(b.v_pool, device),
@@ -296,7 +296,7 @@ def ragged_setup(device):
     """Ragged prefill with a custom mask: packbits of the boolean mask, then
     attention over ragged K/V (8 requests, 32/32 heads)."""
     import paged_kv_attention_plan_gb300 as pka
-    from paged_kv_attention_plan_gb300 import workloads as W
+    from inputs import workloads as W
 
     b = W.ragged_custom_mask(seed=1004)
     d = dict(batch=b, q=bf16(b.q, device), k=bf16(b.k_pool, device), v=bf16(b.v_pool, device))
@@ -325,7 +325,7 @@ def mixed_setup(device, page_size, layout):
     """Mixed serving step: 8 long + 120 short decodes and 4 prefill chunks of
     512 tokens in one plan (decode kernel, tensor-core kernel, merge)."""
     import paged_kv_attention_plan_gb300 as pka
-    from paged_kv_attention_plan_gb300 import workloads as W
+    from inputs import workloads as W
 
     b = W.mixed_step(seed=1003, page_size=page_size, layout=layout, with_payload=False)
     pool = int(b.extra["pool_pages"])
@@ -360,7 +360,7 @@ def cascade_setup(device):
     planned as a two-level cascade and, for comparison, as a flat batch whose
     page tables each list the prompt's pages."""
     import paged_kv_attention_plan_gb300 as pka
-    from paged_kv_attention_plan_gb300 import workloads as W
+    from inputs import workloads as W
 
     c = W.shared_prompt_decode(with_payload=False)
     root, own = c.levels
@@ -416,7 +416,7 @@ def oracle_sample(seconds_budget=20.0, max_requests=None):
     order (wrapping around after the last) until the time budget is spent or
     max_requests have run."""
     from oracle import ref
-    from paged_kv_attention_plan_gb300 import workloads as W
+    from inputs import workloads as W
     b = W.batch_decode(seed=1001)
     done_bytes, t_used, r = 0, 0.0, 0
     limit = max_requests or 1 << 30
@@ -618,16 +618,38 @@ def main():
                             "kernel": "prefill_kernel<128>",
                             "peak_source": pk["source"]},
                "plan": pf["info"].as_dict()}
+    app_gbs = pf["append_bytes"] / (app_ms * 1e-3) / 1e9
+    append_roof = {"bound": "hbm", "achieved": app_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                   "frac": app_gbs / pk["hbm_gbs"], "bytes_per_launch": pf["append_bytes"],
+                   "bytes_counted": "K and V rows of the appended tokens, read once and "
+                                    "written once (2 * 2 * nnz * Hk * D * 2 B)",
+                   "traffic": recorded_traffic("append_kernel append_prefill"),
+                   "kernel": "append_kernel (append_paged_kv_cache)",
+                   "peak_source": pk["source"]}
     del pf
     rg = ragged_setup(device)
     rg_ms = statistics.median(time_steps(lambda: ragged_step(rg), 50, 5, stream))
+    import paged_kv_attention_plan_gb300 as pka
+    pka.pka_packbits(rg["bools"], rg["packed"])
+    rg_attn_ms = statistics.median(time_steps(
+        lambda: rg["attn"].run(rg["q"], rg["k"], rg["v"], None, rg["packed"], out=rg["o"],
+                               lse=rg["lse"]), 50, 5, stream))
+    rg_tf = rg["flops_all"] / (rg_attn_ms * 1e-3) / 1e12
     ragged = {"workload": "ragged_custom_mask: 8 req, qo=kv U[256,2048] (seed 1004), 32/32 "
                           "heads, D 128, ragged K/V, Bernoulli(0.5) OR causal mask; packbits "
                           "then attention",
-              "ms_per_step": rg_ms,
+              "ms_per_step": rg_ms, "attn_ms": rg_attn_ms,
               "tflops_all_pairs": rg["flops_all"] / (rg_ms * 1e-3) / 1e12,
               "tflops_visible_pairs": rg["flops_visible"] / (rg_ms * 1e-3) / 1e12,
-              "unit": "TFLOP/s"}
+              "unit": "TFLOP/s",
+              "roofline": {"bound": "tensor", "achieved": rg_tf, "peak": pk["bf16_tflops"],
+                           "unit": "TFLOP/s", "frac": rg_tf / pk["bf16_tflops"],
+                           "flops_per_launch": rg["flops_all"],
+                           "flops_counted": "4*D*Hq per (query, key) pair over all pairs "
+                                            "(every 128x128 tile has visible keys)",
+                           "traffic": recorded_traffic("prefill_kernel<128> ragged_custom_mask"),
+                           "kernel": "prefill_kernel<128> (custom mask, ragged K/V)",
+                           "peak_source": pk["source"]}}
     del rg
     torch.cuda.empty_cache()
 
@@ -686,7 +708,10 @@ def main():
                        "kv_bytes_per_step": d["kv_bytes"], "bytes_per_step": d["bytes"],
                        "l2": "inputs (604 MB of K/V) larger than L2; no flush",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roof, "fp8_kv_decode": fp8_decode, "tensor_core_decode": tc_decode,
+            "roofline": roof,
+            "roofline_prefill": prefill["roofline"], "roofline_append": append_roof,
+            "roofline_ragged_custom_mask": ragged["roofline"],
+            "fp8_kv_decode": fp8_decode, "tensor_core_decode": tc_decode,
             "prefill": prefill,
             "ragged_custom_mask": ragged,
             "mixed_step": mixed, "cascade": cascade, "e2e": e2e,

@@ -181,9 +181,11 @@ def make_paged_batch(seed, qo_lens, kv_lens, *, page_size, layout=NHD, hq=32, hk
                      mask_mode="causal", pool_pages=None, page_ids=None, name="paged",
                      is_decode=False, with_payload=True, append_new=False, kv_dtype="bf16",
                      k_scale=1.0, v_scale=1.0):
-    """Generic paged batch.  With ``append_new`` the last ``qo_len`` positions
-    of every request are left as NaN in the pool and their rows are returned in
-    ``k_new``/``v_new`` instead (they are what append_paged_kv_cache writes)."""
+    """Generic paged batch.  With ``append_new`` only the cached prefix of
+    every request (its first ``kv_len - qo_len`` positions) is written into
+    the pool; the slots of its last ``qo_len`` positions stay NaN, and the
+    rows append_paged_kv_cache will write there are drawn separately into
+    ``k_new``/``v_new`` ([nnz_q, Hk, D] bf16 bits)."""
     rng = np.random.default_rng(seed)
     qo_lens = np.asarray(qo_lens, dtype=np.int32)
     kv_lens = np.asarray(kv_lens, dtype=np.int32)
@@ -197,27 +199,12 @@ def make_paged_batch(seed, qo_lens, kv_lens, *, page_size, layout=NHD, hq=32, hk
     b.extra["pool_pages"] = pool
     if with_payload:
         b.q = normal_bf16_bits(rng, (b.nnz_q, hq, d))
-        b.k_pool, b.v_pool = fill_pool(rng, kv_lens, kv_indptr, kv_indices, page_size, pool,
+        filled = kv_lens - qo_lens if append_new else kv_lens
+        b.k_pool, b.v_pool = fill_pool(rng, filled, kv_indptr, kv_indices, page_size, pool,
                                        hk, d, layout, kv_dtype)
         if append_new:
-            b.k_new = np.empty((b.nnz_q, hk, d), dtype=np.uint16)
-            b.v_new = np.empty((b.nnz_q, hk, d), dtype=np.uint16)
-            for r in range(len(kv_lens)):
-                q0, q1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
-                for t in range(q1 - q0):
-                    pos = int(kv_lens[r]) - (q1 - q0) + t
-                    pg = int(kv_indices[kv_indptr[r] + pos // page_size])
-                    s = pos % page_size
-                    if layout == NHD:
-                        b.k_new[q0 + t] = b.k_pool[pg, s]
-                        b.v_new[q0 + t] = b.v_pool[pg, s]
-                        b.k_pool[pg, s] = BF16_NAN_BITS
-                        b.v_pool[pg, s] = BF16_NAN_BITS
-                    else:
-                        b.k_new[q0 + t] = b.k_pool[pg, :, s]
-                        b.v_new[q0 + t] = b.v_pool[pg, :, s]
-                        b.k_pool[pg, :, s] = BF16_NAN_BITS
-                        b.v_pool[pg, :, s] = BF16_NAN_BITS
+            b.k_new = normal_bf16_bits(rng, (b.nnz_q, hk, d))
+            b.v_new = normal_bf16_bits(rng, (b.nnz_q, hk, d))
     return b
 
 

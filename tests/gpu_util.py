@@ -81,3 +81,24 @@ def assert_parity(o, lse, o_ref, lse_ref, rows=None):
             e = np.abs(lse[fin] - lse_ref[fin]).max()
             assert e <= LSE_MAX, f"LSE max abs error {e:.3e}"
         assert np.all(lse[~fin] == lse_ref[~fin])
+
+
+def plan_item_rows(attn):
+    """Global query rows at both ends of every work item of the plan `attn`
+    holds, read from its plan image: each decode item's row, and the first
+    and last token of every 128-row query tile of every tensor-core item.
+    Comparing these rows with the oracle touches every item of the real plan,
+    every split piece and the first and last item of every CTA."""
+    from tests.plan_image import parse
+    pka.pka_plan_wait(attn.handle)
+    img = parse(attn.pinned.numpy()[: int(attn.info.int_ws_bytes)])
+    g = attn.params.num_qo_heads // attn.params.num_kv_heads
+    tq = 128 // g
+    rows = set()
+    for w in img["decode_items"]:
+        rows.add(w["q_row0"])
+    for w in img["prefill_items"]:
+        for t0 in range(0, w["q_count"], tq):
+            rows.add(w["q_row0"] + t0)
+            rows.add(w["q_row0"] + min(t0 + tq, w["q_count"]) - 1)
+    return rows

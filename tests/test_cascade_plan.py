@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import paged_kv_attention_plan_gb300 as pka
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 from tests.plan_image import parse
 
 OK, INVALID, METADATA, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3, 4

@@ -13,7 +13,7 @@ import torch
 
 import paged_kv_attention_plan_gb300 as pka
 from oracle import ref
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 from tests.gpu_util import assert_parity, bf16, f64, i32
 
 pytestmark = pytest.mark.gpu

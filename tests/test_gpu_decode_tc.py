@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 from oracle import ref
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 from tests.gpu_util import assert_parity, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu

@@ -8,7 +8,7 @@ ragged K/V, and the 64-request batch-decode workload at full size.
 import numpy as np
 import pytest
 
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 from tests.gpu_util import assert_parity, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu

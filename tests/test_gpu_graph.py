@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import paged_kv_attention_plan_gb300 as pka
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 from tests.gpu_util import assert_parity, bf16, f64, i32, run_oracle
 
 pytestmark = pytest.mark.gpu

@@ -13,8 +13,8 @@ import torch
 
 import paged_kv_attention_plan_gb300 as pka
 from oracle import ref
-from paged_kv_attention_plan_gb300 import workloads as W
-from tests.gpu_util import assert_parity, bf16, f64, i32, run_gpu, run_oracle
+from inputs import workloads as W
+from tests.gpu_util import assert_parity, bf16, f64, i32, plan_item_rows, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -123,7 +123,10 @@ def test_append_prefill_full_size():
                                        kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
                                        last_page_len=b.last_page_len, page_size=16)
     b.k_pool, b.v_pool = kr, vr
-    rows = _sample_rows(b)
+    # both ends of every query tile of every work item, plus random rows
+    rows = _sample_rows(b) | plan_item_rows(attn)
+    print(f"append_prefill: {len(rows)} of {b.nnz_q} rows compared with the oracle "
+          f"({attn.info.num_prefill_items} items, {attn.info.num_prefill_ctas} CTAs)")
     o_ref, lse_ref = run_oracle(b, rows=rows)
     assert_parity(f64(o), f64(lse), o_ref, lse_ref, rows=rows)
 
@@ -136,8 +139,11 @@ def test_ragged_custom_mask_full_size():
     torch.cuda.synchronize()
     packed_ref = ref.packbits_little(b.mask_bool)
     assert np.array_equal(packed.cpu().numpy(), packed_ref)
-    o, lse, _ = run_gpu(b, ("auto", 1), packed_mask=packed_ref)
-    rows = _sample_rows(b, per_req=2)
+    attn = pka.BatchAttention()
+    o, lse, _ = run_gpu(b, ("auto", 1), packed_mask=packed_ref, attn=attn)
+    rows = _sample_rows(b, per_req=2) | plan_item_rows(attn)
+    print(f"ragged_custom_mask: {len(rows)} of {b.nnz_q} rows compared with the oracle "
+          f"({attn.info.num_prefill_items} items, {attn.info.num_prefill_ctas} CTAs)")
     o_ref, lse_ref = run_oracle(b, packed_mask=packed_ref, rows=rows)
     assert_parity(o, lse, o_ref, lse_ref, rows=rows)
 
@@ -145,11 +151,11 @@ def test_ragged_custom_mask_full_size():
 @pytest.mark.parametrize("page_size,layout", [(1, "NHD"), (16, "HND")])
 def test_mixed_step_full_size(page_size, layout):
     """8 long decodes (32K-131K keys), 120 short decodes and 4 prefill chunks of
-    512 tokens in one plan; decode rows and prefill rows sampled."""
-    from paged_kv_attention_plan_gb300 import workloads as Wk
+    512 tokens in one plan; every decode row and both ends of every query tile
+    of the tensor-core items against the oracle."""
+    from inputs import workloads as Wk
     b = Wk.mixed_step(page_size=page_size, layout=layout, with_payload=False)
-    rng = np.random.default_rng(5)
-    # payload drawn on the host only for the pages the sampled rows read
+    # payload drawn on the device (seeded), then copied to the host for the oracle
     hk, d = 8, 128
     pool = int(b.extra["pool_pages"])
     shape = (pool, page_size, hk, d) if layout == "NHD" else (pool, hk, page_size, d)
@@ -164,21 +170,18 @@ def test_mixed_step_full_size(page_size, layout):
     o, lse = attn.run(q, k, v, i32(b.kv_indices))
     torch.cuda.synchronize()
     assert pka.pka_get_device_error() == 0
-    # sampled rows: 2 long decodes, 3 short decodes, first/last rows of 2 chunks
-    reqs = [0, 7, 8, 60, 127, 128, 131]
-    rows = set()
-    for r in reqs:
+    # every decode row (each split piece's row among them), both ends of every
+    # query tile of every tensor-core item, and the last row of every chunk
+    rows = plan_item_rows(attn)
+    for r in range(b.batch_size):
         q0, q1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
         rows.update({q0, q1 - 1})
-    # copy only the pages of the sampled requests to the host
+    print(f"mixed_step page {page_size}: {len(rows)} of {b.nnz_q} rows compared with the "
+          f"oracle ({info.num_decode_items} decode items, {info.num_prefill_items} tensor-core "
+          f"items, {info.num_merge_tasks} merge tasks)")
     b.q = q.view(torch.int16).cpu().numpy().view(np.uint16)
-    page_ids = np.concatenate([b.kv_indices[b.kv_indptr[r]:b.kv_indptr[r + 1]] for r in reqs])
-    kh = np.zeros(shape, np.uint16)
-    vh = np.zeros(shape, np.uint16)
-    idx = torch.from_numpy(page_ids.astype(np.int64)).cuda()
-    kh[page_ids] = k.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
-    vh[page_ids] = v.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
-    b.k_pool, b.v_pool = kh, vh
+    b.k_pool = k.view(torch.int16).cpu().numpy().view(np.uint16)
+    b.v_pool = v.view(torch.int16).cpu().numpy().view(np.uint16)
     o_ref, lse_ref = run_oracle(b, rows=rows)
     assert_parity(f64(o), f64(lse), o_ref, lse_ref, rows=rows)
 

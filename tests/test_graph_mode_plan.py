@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import paged_kv_attention_plan_gb300 as pka
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 from tests.plan_image import parse
 from tests.test_host_abi import SMALL, check_coverage
 

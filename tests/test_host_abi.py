@@ -16,7 +16,7 @@ import pytest
 
 import paged_kv_attention_plan_gb300 as pka
 from paged_kv_attention_plan_gb300 import _pka
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 from tests.plan_image import parse
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -471,3 +471,68 @@ def test_empty_batches_plan_to_nothing(qo, kv, last):
     pka.pka_plan_destroy(h)
     assert info.nnz_qo == 0 and info.num_decode_items == 0 and info.num_prefill_items == 0
     assert info.float_ws_bytes == 0 and info.num_merge_tasks == 0
+
+
+@pytest.mark.parametrize("arrive,polls", [(2, 10), (-1, 10), (0, 0), (1, 1001), (0, -5)])
+def test_wait_selftest_rejects_bad_arguments(arrive, polls):
+    """Checked before any launch, so no GPU is needed."""
+    assert _pka.lib().pka_selftest_bounded_wait(arrive, polls, None) == INVALID
+
+
+# ---------------------------------------------------------------------------
+# pka_check_indices: page ids against the pool, appended slots against other
+# requests ("Deep Dive - FlashInfer", "Where FlashInfer sits in a serving
+# stack": reused pages and page tables that disagree with last_page_len)
+# ---------------------------------------------------------------------------
+
+def _check(kv, idx, last, pool, app=None, P=4):
+    return pka.pka_check_indices(_p(page_size=P), _i32(kv), _i32(idx), _i32(last), pool,
+                                 None if app is None else _i32(app))
+
+
+def test_check_indices_accepts_the_worked_batch():
+    # printed page ids [7, 2], [11], [3, 14, 6] in a 15-page pool, appends 3/1/4
+    assert _check([0, 2, 3, 6], [7, 2, 11, 3, 14, 6], [2, 2, 1], 15) == (OK, -1)
+    assert _check([0, 2, 3, 6], [7, 2, 11, 3, 14, 6], [2, 2, 1], 15, app=[0, 3, 4, 8]) == (OK, -1)
+
+
+@pytest.mark.parametrize("bad_at,value", [(0, -1), (4, 15), (5, 1 << 30)])
+def test_check_indices_rejects_ids_outside_the_pool(bad_at, value):
+    idx = [7, 2, 11, 3, 14, 6]
+    idx[bad_at] = value
+    assert _check([0, 2, 3, 6], idx, [2, 2, 1], 15) == (METADATA, bad_at)
+
+
+def test_check_indices_rejects_two_requests_appending_one_slot():
+    # both requests end in page 5; request 0 appends slots 1..2 of it (kv 7, last 3),
+    # request 1 appends slot 2 of it (kv 3 in one page, appends 1: position 2)
+    s, bad = _check([0, 2, 3], [4, 5, 5], [3, 3], 8, app=[0, 2, 3])
+    assert s == METADATA and bad == 2
+
+
+def test_check_indices_rejects_appending_into_another_requests_history():
+    # request 1 reads page 5 slots 0..2 as history; request 0 appends slot 1 of page 5
+    s, bad = _check([0, 2, 3], [4, 5, 5], [2, 4], 8, app=[0, 1, 2])
+    assert s == METADATA and bad == 2
+
+
+def test_check_indices_allows_a_shared_read_only_prefix():
+    # pages 1, 2 hold a shared prefix read by both requests; each appends into its own page
+    assert _check([0, 3, 6], [1, 2, 3, 1, 2, 4], [2, 3], 5, app=[0, 2, 5]) == (OK, -1)
+
+
+def test_check_indices_argument_errors():
+    assert _check([0, 2, 3, 6], [7, 2, 11, 3, 14], [2, 2, 1], 15)[0] == INVALID  # short indices
+    assert _check([0, 2, 3, 6], [7, 2, 11, 3, 14, 6], [2, 5, 1], 15)[0] == METADATA  # last > P
+    assert _check([0, 2, 3, 6], [7, 2, 11, 3, 14, 6], [2, 2, 1], 15,
+                  app=[0, 9, 10, 11])[0] == METADATA  # appends beyond kv_len
+    assert _check([0], [], [], 0) == (OK, -1)  # empty batch
+
+
+def test_check_indices_seeded_workloads_are_clean():
+    for b in (W.worked_example(), W.append_prefill(with_payload=False),
+              W.mixed_step(page_size=16, layout="HND", with_payload=False)):
+        s, bad = pka.pka_check_indices(_p(page_size=b.page_size), b.kv_indptr, b.kv_indices,
+                                       b.last_page_len, int(b.extra["pool_pages"]),
+                                       b.qo_indptr)
+        assert (s, bad) == (OK, -1), b.name

@@ -24,7 +24,7 @@ import pytest
 import torch
 
 from oracle import ref
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 
 
 def _run(b, **kw):

@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 from oracle import ref
-from paged_kv_attention_plan_gb300 import workloads as W
+from inputs import workloads as W
 
 
 def test_e4m3_fixed_points():

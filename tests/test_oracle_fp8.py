@@ -168,3 +168,68 @@ def test_quantizing_append_round_trip():
         assert np.array_equal(rows[-(q1 - q0):], want_k[q0:q1])
     touched = ko != W.E4M3_NAN_CODE
     assert touched.sum() <= b.k_new.size and (vo != W.E4M3_NAN_CODE).sum() <= b.v_new.size
+
+
+# ---------------------------------------------------------------------------
+# Rows with qo_len >= 2 over e4m3 pools (append / prefill): the same reading,
+# one scale per pool, for every row length and mask mode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout,page_size", [("HND", 16), ("NHD", 4), ("HND", 1)])
+@pytest.mark.parametrize("mask_mode", ["causal", "none"])
+def test_fp8_prefill_rows_equal_bf16_of_decoded_values(layout, page_size, mask_mode):
+    b = W.make_paged_batch(8, [5, 1, 33, 2], [9, 30, 40, 2], page_size=page_size, layout=layout,
+                           hq=8, hk=2, d=64, mask_mode=mask_mode, kv_dtype="e4m3",
+                           k_scale=0.5, v_scale=4.0)
+    kw = dict(qo_indptr=b.qo_indptr, kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+              last_page_len=b.last_page_len, page_size=page_size, num_qo_heads=8,
+              num_kv_heads=2, layout=layout, mask_mode=mask_mode)
+    o8, l8 = ref.batch_attention(b.q, b.k_pool, b.v_pool, kv_dtype="e4m3", k_scale=0.5,
+                                 v_scale=4.0, **kw)
+    o16, l16 = ref.batch_attention(b.q, _bf16_copy(b.k_pool, 0.5), _bf16_copy(b.v_pool, 4.0), **kw)
+    assert np.all(np.isfinite(o8))
+    assert np.allclose(o8, o16, rtol=0, atol=1e-12)
+    assert np.allclose(l8, l16, rtol=0, atol=1e-12)
+
+
+def test_fp8_prefill_custom_mask_equals_bf16_of_decoded_values():
+    b = W.make_paged_batch(9, [6, 3], [10, 7], page_size=4, layout="HND", hq=4, hk=4, d=64,
+                           mask_mode="custom", kv_dtype="e4m3", k_scale=2.0, v_scale=0.25)
+    rng = np.random.default_rng(9)
+    bits = np.concatenate([(rng.random((q, k)) < 0.6).reshape(-1)
+                           for q, k in zip(b.qo_lens, b.kv_lens)])
+    packed = ref.packbits_little(bits)
+    kw = dict(qo_indptr=b.qo_indptr, kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+              last_page_len=b.last_page_len, page_size=4, num_qo_heads=4, num_kv_heads=4,
+              layout="HND", mask_mode="custom", packed_mask=packed)
+    o8, l8 = ref.batch_attention(b.q, b.k_pool, b.v_pool, kv_dtype="e4m3", k_scale=2.0,
+                                 v_scale=0.25, **kw)
+    o16, l16 = ref.batch_attention(b.q, _bf16_copy(b.k_pool, 2.0), _bf16_copy(b.v_pool, 0.25),
+                                   **kw)
+    assert np.allclose(o8, o16, rtol=0, atol=1e-12, equal_nan=False)
+    fin = np.isfinite(l16)
+    assert np.array_equal(fin, np.isfinite(l8)) and np.allclose(l8[fin], l16[fin], atol=1e-12)
+
+
+def test_fp8_appended_prefill_attends_to_quantized_rows():
+    """Append into e4m3 pools, then attend: the new rows the attention sees
+    are the quantized rows (value / scale rounded to e4m3, times scale)."""
+    b = W.make_paged_batch(10, [4, 3], [9, 3], page_size=4, layout="HND", hq=4, hk=2, d=64,
+                           append_new=True)
+    shape = b.k_pool.shape
+    k8 = np.full(shape, W.E4M3_NAN_CODE, np.uint8)
+    v8 = np.full(shape, W.E4M3_NAN_CODE, np.uint8)
+    fin = ~np.isnan(ref.bf16_bits_to_f64(b.k_pool))
+    k8[fin] = ref.quantize_kv_e4m3(b.k_pool[fin], 0.5)
+    v8[fin] = ref.quantize_kv_e4m3(b.v_pool[fin], 2.0)
+    ko, vo = ref.append_paged_kv_cache(b.k_new, b.v_new, b.qo_indptr, k8, v8,
+                                       kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+                                       last_page_len=b.last_page_len, page_size=4, layout="HND",
+                                       kv_dtype="e4m3", k_scale=0.5, v_scale=2.0)
+    kw = dict(qo_indptr=b.qo_indptr, kv_indptr=b.kv_indptr, kv_indices=b.kv_indices,
+              last_page_len=b.last_page_len, page_size=4, num_qo_heads=4, num_kv_heads=2,
+              layout="HND")
+    o8, l8 = ref.batch_attention(b.q, ko, vo, kv_dtype="e4m3", k_scale=0.5, v_scale=2.0, **kw)
+    o16, l16 = ref.batch_attention(b.q, _bf16_copy(ko, 0.5), _bf16_copy(vo, 2.0), **kw)
+    assert np.all(np.isfinite(o8))
+    assert np.allclose(o8, o16, rtol=0, atol=1e-12) and np.allclose(l8, l16, rtol=0, atol=1e-12)

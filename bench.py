@@ -282,6 +282,31 @@ def prefill_setup(device):
     return d
 
 
+def prefill_fp8_setup(device):
+    """The append-prefill workload over e4m3 pools (HND, page 16, k_scale 0.5,
+    v_scale 2): append_paged_kv_cache quantizes the new rows into the pools,
+    then attention (the tensor-core rows' keys decoded to a bf16 scratch)."""
+    import paged_kv_attention_plan_gb300 as pka
+    from inputs import workloads as W
+
+    b = W.append_prefill(seed=1002, layout="HND", kv_dtype="e4m3", k_scale=0.5, v_scale=2.0)
+    d = dict(batch=b, q=bf16(b.q, device), k=kv_tensor(b.k_pool, device),
+             v=kv_tensor(b.v_pool, device), k_new=bf16(b.k_new, device),
+             v_new=bf16(b.v_new, device), idx=i32(b.kv_indices, device),
+             qo=i32(b.qo_indptr, device), kvp=i32(b.kv_indptr, device),
+             last=i32(b.last_page_len, device))
+    kw = dict(layout="HND", kv_dtype="e4m3", k_scale=0.5, v_scale=2.0)
+    d["params"] = pka.make_params(32, 8, 128, 16, **kw)
+    attn = pka.BatchAttention(device=device)
+    d["info"] = attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, num_qo_heads=32,
+                          num_kv_heads=8, head_dim=128, page_size=16, split_mode="auto", **kw)
+    d["attn"] = attn
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty(b.nnz_q, 32, dtype=torch.float32, device=device)
+    d["flops"] = prefill_flops(b)
+    return d
+
+
 def prefill_append(d):
     import paged_kv_attention_plan_gb300 as pka
     pka.pka_append_paged_kv_cache(d["params"], d["k_new"], d["v_new"], d["qo"], d["kvp"], d["idx"],
@@ -479,8 +504,8 @@ def profile_one(name, device, stream, steps, warmup, pk):
         ms = time_steps(lambda: decode_step(d), steps, warmup, stream)
         out = {"workload": "batch_decode", "ms": statistics.median(ms),
                "GB/s": d["bytes"] / (statistics.median(ms) * 1e-3) / 1e9}
-    elif name == "prefill":
-        d = prefill_setup(device)
+    elif name in ("prefill", "prefill_fp8"):
+        d = prefill_setup(device) if name == "prefill" else prefill_fp8_setup(device)
         ms = time_steps(lambda: (prefill_append(d), prefill_attn(d)), steps, warmup, stream)
         out = {"workload": "append_prefill", "ms": statistics.median(ms),
                "TFLOP/s": d["flops"] / (statistics.median(ms) * 1e-3) / 1e12}
@@ -509,8 +534,8 @@ def main():
     ap.add_argument("--impl", default="pka", choices=["pka", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="all",
-                    choices=["all", "decode", "decode_fp8", "decode_tc", "prefill", "ragged",
-                             "mixed1", "mixed16", "cascade"],
+                    choices=["all", "decode", "decode_fp8", "decode_tc", "prefill", "prefill_fp8",
+                             "ragged", "mixed1", "mixed16", "cascade"],
                     help="all (default) prints the benchmark line; a single workload only runs "
                          "that workload's kernels (for profiling) and prints its numbers")
     args = ap.parse_args()
@@ -627,6 +652,22 @@ def main():
                    "kernel": "append_kernel (append_paged_kv_cache)",
                    "peak_source": pk["source"]}
     del pf
+    torch.cuda.empty_cache()
+    # ---- the same append-prefill batch over e4m3 pools
+    pf8 = prefill_fp8_setup(device)
+    f8_attn_ms = statistics.median(time_steps(lambda: prefill_attn(pf8), 50, 5, stream))
+    f8_step_ms = statistics.median(time_steps(lambda: (prefill_append(pf8), prefill_attn(pf8)),
+                                              50, 5, stream))
+    prefill_fp8 = {"workload": "append_prefill over e4m3 K/V (HND, page 16, k_scale 0.5, "
+                               "v_scale 2): append_paged_kv_cache quantizes the new rows, then "
+                               "attention (keys of the tensor-core rows decoded to a bf16 "
+                               "scratch, then the tcgen05 kernel)",
+                   "attn_ms": f8_attn_ms, "ms_per_step": f8_step_ms,
+                   "tflops_attn": pf8["flops"] / (f8_attn_ms * 1e-3) / 1e12,
+                   "value": pf8["flops"] / (f8_step_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                   "kv_scratch_rows": pf8["info"].kv_scratch_rows}
+    del pf8
+    torch.cuda.empty_cache()
     rg = ragged_setup(device)
     rg_ms = statistics.median(time_steps(lambda: ragged_step(rg), 50, 5, stream))
     import paged_kv_attention_plan_gb300 as pka
@@ -711,7 +752,8 @@ def main():
             "roofline": roof,
             "roofline_prefill": prefill["roofline"], "roofline_append": append_roof,
             "roofline_ragged_custom_mask": ragged["roofline"],
-            "fp8_kv_decode": fp8_decode, "tensor_core_decode": tc_decode,
+            "fp8_kv_decode": fp8_decode, "fp8_kv_append_prefill": prefill_fp8,
+            "tensor_core_decode": tc_decode,
             "prefill": prefill,
             "ragged_custom_mask": ragged,
             "mixed_step": mixed, "cascade": cascade, "e2e": e2e,

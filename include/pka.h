@@ -78,8 +78,12 @@ typedef enum pka_mask_mode {
  * bits); code c of the K pool stands for e4m3(c) * k_scale, of the V pool for
  * e4m3(c) * v_scale.  The pages tie low-precision caches to the HND layout
  * ("KV-Cache layouts", "NHD/HND") but fix no scale contract: one scale per
- * pool is the plainest reading.  Decode rows only (qo_len == 1), any layout
- * and page size; page_stride (in elements = bytes) a multiple of 16. */
+ * pool is the plainest reading.  Any layout and page size; page_stride (in
+ * elements = bytes) a multiple of 16.  Decode rows read the codes directly;
+ * for rows with qo_len >= 2 (tensor cores) run() first decodes each such
+ * request's keys to bf16 (exact) into a scratch in the float workspace
+ * (info.kv_scratch_rows rows of K and of V), then reads that scratch.  Not
+ * in graph mode or cascades for rows with qo_len >= 2. */
 typedef enum pka_kv_dtype { PKA_KV_BF16 = 0, PKA_KV_FP8_E4M3 = 1 } pka_kv_dtype;
 typedef enum pka_split_mode {
   PKA_SPLIT_OFF = 0,    /* one work item per (request, head block, q tile)   */
@@ -138,7 +142,9 @@ typedef struct pka_plan_info {
   int32_t num_decode_joins;  /* split (decode row, kv head) pairs that the     */
                              /* decode kernel merges itself (their g qo heads  */
                              /* are among num_merge_tasks)                     */
-  int32_t reserved[4];
+  int32_t kv_scratch_rows;   /* e4m3 K/V: bf16 rows decoded for the tensor-core */
+                             /* rows in the float workspace (0 otherwise)       */
+  int32_t reserved[3];
 } pka_plan_info;
 
 typedef struct pka_plan_s* pka_plan_t;
@@ -153,9 +159,8 @@ pka_status pka_version(int32_t* major, int32_t* minor);
  * qo_indptr_h may be NULL (decode: one row per request).  Host only; needs
  * no GPU.  Returns PKA_ERR_METADATA for: indptr[0] != 0, a decreasing
  * indptr, a request with no page, last_page_len outside 1..P, causal rows
- * with kv_len < qo_len; PKA_ERR_UNSUPPORTED for head_dim not in {64,128}, a
- * head ratio not in {1,2,4,8}, or e4m3 K/V with rows of qo_len >= 2;
- * PKA_ERR_INVALID_ARG for bad enums or sizes. */
+ * with kv_len < qo_len; PKA_ERR_UNSUPPORTED for head_dim not in {64,128} or a
+ * head ratio not in {1,2,4,8}; PKA_ERR_INVALID_ARG for bad enums or sizes. */
 pka_status pka_validate(const pka_params* params, int32_t batch, const int32_t* qo_indptr_h,
                         const int32_t* kv_indptr_h, const int32_t* last_page_len_h);
 

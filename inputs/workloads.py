@@ -343,15 +343,18 @@ def batch_decode(seed=1001, n=64, kv_lo=512, kv_hi=4096, page_size=16, layout=NH
 
 
 def append_prefill(seed=1002, n=16, q_lo=128, q_hi=1024, prefix_hi=4096, page_size=16,
-                   layout=NHD, hq=32, hk=8, d=128, with_payload=True):
+                   layout=NHD, hq=32, hk=8, d=128, with_payload=True, kv_dtype="bf16",
+                   k_scale=1.0, v_scale=1.0):
     """16 requests, qo_len ~ U[128,1024], cached prefix ~ U[0,4096], causal.
-    New K/V rows come in ``k_new``/``v_new`` for append_paged_kv_cache."""
+    New K/V rows come in ``k_new``/``v_new`` (bf16) for append_paged_kv_cache;
+    with kv_dtype "e4m3" the cached prefix is e4m3 codes."""
     rng = np.random.default_rng(seed)
     ql = rng.integers(q_lo, q_hi, size=n, endpoint=True)
     pre = rng.integers(0, prefix_hi, size=n, endpoint=True)
     return make_paged_batch(seed + 7, ql, pre + ql, page_size=page_size, layout=layout, hq=hq,
                             hk=hk, d=d, mask_mode="causal", name="append_prefill",
-                            with_payload=with_payload, append_new=with_payload)
+                            with_payload=with_payload, append_new=with_payload,
+                            kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale)
 
 
 def mixed_step(seed=1003, page_size=1, layout=NHD, n_long=8, long_lo=32768, long_hi=131072,

@@ -53,7 +53,7 @@ class pka_plan_info(ctypes.Structure):
                 ("num_prefill_items", ctypes.c_int32), ("num_merge_tasks", ctypes.c_int32),
                 ("num_partial_records", ctypes.c_int32),
                 ("decode_chunk_tokens", ctypes.c_int32), ("num_decode_joins", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 4)]
+                ("kv_scratch_rows", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}

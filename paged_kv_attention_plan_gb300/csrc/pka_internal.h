@@ -111,6 +111,10 @@ cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_
                           const int32_t* last_page_len, void* k, void* v,
                           int64_t page_stride, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int arrive, int polls, cudaStream_t stream);
+cudaError_t launch_dequant(const PkaDequantUnit* units, int n_units, int64_t rows,
+                           const int32_t* kv_indices, const void* k8, const void* v8,
+                           int64_t page_stride, int page_size, int layout, int ragged, int hk,
+                           int d, uint16_t* out_k, uint16_t* out_v, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
 // Device address of the error word on the current device (null on failure).
 int32_t* device_error_word();

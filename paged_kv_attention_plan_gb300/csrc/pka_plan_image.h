@@ -3,8 +3,8 @@
 // host planner and the kernels (both are the product path).
 //
 // image := header | decode_cta_ptr | decode_items | prefill_cta_ptr |
-//          prefill_items | merge_tasks | merge_slots | decode_joins
-//          (offsets in int32 units)
+//          prefill_items | merge_tasks | merge_slots | decode_joins |
+//          dequant_units (offsets in int32 units)
 #pragma once
 #include <stdint.h>
 
@@ -29,7 +29,10 @@ struct PkaImageHeader {
   int32_t off_merge_slots;       // int32[num_partial_records] record lists, 0 if none
   int32_t num_decode_joins;      // split decode (request, kv head) pairs merged in the decode kernel
   int32_t off_decode_joins;      // PkaDecodeJoin[num_decode_joins], 0 if none
-  int32_t reserved[14];
+  int32_t num_dequant_units;     // e4m3 K/V: requests whose keys the tensor-core rows read
+  int32_t off_dequant_units;     // PkaDequantUnit[num_dequant_units], 0 if none
+  int32_t dequant_rows;          // rows of the bf16 K/V scratch (sum of their kv_len)
+  int32_t reserved[11];
 };
 
 // One unit of attention work: a block of kv heads (decode) or one kv head
@@ -77,6 +80,17 @@ struct PkaDecodeJoin {
   int32_t rec_stride;  // records between consecutive pieces
 };
 
+// e4m3 K/V, one request whose keys the tensor-core rows read: its logical
+// keys 0 .. kv_len - 1 (page ids from kv_base in kv_indices) are decoded to
+// bf16 rows dst_row0 .. dst_row0 + kv_len - 1 of a [rows, Hk, D] scratch in
+// the float workspace, which those rows then read as ragged K/V.
+struct PkaDequantUnit {
+  int32_t kv_base;   // first page id slot of the request in kv_indices
+  int32_t kv_len;    // its keys
+  int32_t dst_row0;  // first scratch row
+  int32_t reserved;
+};
+
 // Item flags
 #define PKA_ITEM_ALL_VISIBLE 1  // every key of the range is visible (cascade levels above the last)
 
@@ -84,3 +98,4 @@ static_assert(sizeof(PkaImageHeader) == 128, "header size");
 static_assert(sizeof(PkaDecodeJoin) == 16, "join size");
 static_assert(sizeof(PkaWorkItem) == 64, "work item size");
 static_assert(sizeof(PkaMergeTask) == 32, "merge task size");
+static_assert(sizeof(PkaDequantUnit) == 16, "dequant unit size");

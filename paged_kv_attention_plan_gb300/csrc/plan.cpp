@@ -39,6 +39,10 @@ struct PlanLists {
   struct Slot { int32_t row, head, rec; };
   std::vector<Slot> slots;
   std::vector<int32_t> merge_slots;
+  // e4m3 K/V: requests whose keys are decoded to bf16 for the tensor-core rows
+  std::vector<PkaDequantUnit> dequant;
+  std::vector<int32_t> dequant_row0;  // per request: its first scratch row, or -1
+  int64_t dequant_rows = 0;
 
   void reset(bool is_cascade) {
     dec_cta_ptr.assign(1, 0);
@@ -51,6 +55,8 @@ struct PlanLists {
     cascade = is_cascade;
     slots.clear();
     merge_slots.clear();
+    dequant.clear();
+    dequant_rows = 0;
   }
 };
 
@@ -206,13 +212,31 @@ pka_status derive(const pka_params* p, int32_t batch, const int32_t* qo, const i
   return PKA_OK;
 }
 
-// e4m3 K/V is read by the decode kernel only: rows with qo_len >= 2 (the
-// tensor-core path) are refused.
+// e4m3 K/V: decode rows read the codes; rows with qo_len >= 2 read a bf16
+// scratch decoded in run(), whose size depends on the batch, so graph mode
+// (fixed workspaces) refuses them.
 pka_status check_kv_dtype(const pka_params* p, const Batch& b) {
-  if (p->kv_dtype != PKA_KV_FP8_E4M3) return PKA_OK;
+  if (p->kv_dtype != PKA_KV_FP8_E4M3 || !graph_mode(p)) return PKA_OK;
   for (int32_t q : b.qo_len)
     if (q >= 2) return PKA_ERR_UNSUPPORTED;
   return PKA_OK;
+}
+
+// e4m3 K/V: one dequant unit per request that tensor-core items read (in
+// request order, scratch rows back to back), and those items' kv_base
+// rewritten to the request's first scratch row (the kernel then reads the
+// scratch as ragged K/V).
+void plan_dequant(const std::vector<Batch>& lv, PlanLists* L) {
+  const Batch& b = lv[0];
+  L->dequant_row0.assign(b.kv_len.size(), -1);
+  for (const PkaWorkItem& w : L->pre_items) L->dequant_row0[w.req] = 0;
+  for (size_t r = 0; r < b.kv_len.size(); ++r) {
+    if (L->dequant_row0[r] < 0) continue;
+    L->dequant_row0[r] = (int32_t)L->dequant_rows;
+    L->dequant.push_back({b.kv_base[r], b.kv_len[r], (int32_t)L->dequant_rows, 0});
+    L->dequant_rows += b.kv_len[r];
+  }
+  for (PkaWorkItem& w : L->pre_items) w.kv_base = L->dequant_row0[w.req];
 }
 
 PkaWorkItem make_item(const Batch& b, int r, int kv_head0, int n_kv_heads, int q_local0,
@@ -585,6 +609,13 @@ void fold_ctas(std::vector<int32_t>& cta_ptr, std::vector<PkaWorkItem>& items, i
 
 size_t align_words(size_t w) { return (w + 15) & ~size_t(15); }
 
+// Bytes of one bf16 K (or V) scratch of `rows` rows [rows, Hk, D], rounded
+// up to 256.
+size_t kv_scratch_bytes(const pka_params* p, int64_t rows) {
+  const size_t b = (size_t)rows * p->num_kv_heads * p->head_dim * 2;
+  return (b + 255) & ~size_t(255);
+}
+
 }  // namespace
 
 void pka::set_last_error(const char* msg) {
@@ -626,6 +657,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   plan_decode(p, lv, num_sms, &L);
   plan_prefill(p, lv, num_sms, &L);
   if (cascade) build_slot_merges(&L, nnz, p->num_qo_heads);
+  if (p->kv_dtype == PKA_KV_FP8_E4M3 && !cascade && !L.pre_items.empty()) plan_dequant(lv, &L);
+  if (L.dequant_rows > INT32_MAX) return PKA_ERR_UNSUPPORTED;
   GraphCaps caps;
   if (graph) {
     caps = graph_caps(p, num_sms);
@@ -675,6 +708,11 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   constexpr size_t kJoinWords = sizeof(PkaDecodeJoin) / 4;
   h.off_decode_joins = n_join > 0 ? (int)w : 0;
   w = align_words(w + n_join * kJoinWords);
+  constexpr size_t kDequantWords = sizeof(PkaDequantUnit) / 4;
+  h.num_dequant_units = (int)L.dequant.size();
+  h.off_dequant_units = L.dequant.empty() ? 0 : (int)w;
+  h.dequant_rows = (int)L.dequant_rows;
+  w = align_words(w + L.dequant.size() * kDequantWords);
   if (w > (size_t)INT32_MAX || layout_records > INT32_MAX / 256) {
     pka::set_last_error("plan image or partial records exceed 2^31");
     return PKA_ERR_UNSUPPORTED;
@@ -687,6 +725,9 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   size_t rec_o_al = (rec_o + 255) & ~size_t(255);
   info.float_ws_bytes =
       layout_records ? rec_o_al + (((size_t)layout_records * 4 + 255) & ~size_t(255)) : 0;
+  // e4m3 K/V: the bf16 K and V scratch follow the partial states
+  info.float_ws_bytes += 2 * kv_scratch_bytes(p, L.dequant_rows);
+  info.kv_scratch_rows = (int32_t)L.dequant_rows;
   info.num_requests = batch;
   info.nnz_qo = nnz;
   info.total_kv = total_kv;
@@ -736,6 +777,9 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
     std::memcpy(img + h.off_merge_slots, L.merge_slots.data(), L.merge_slots.size() * 4);
   if (!L.joins.empty())
     std::memcpy(img + h.off_decode_joins, L.joins.data(), L.joins.size() * sizeof(PkaDecodeJoin));
+  if (!L.dequant.empty())
+    std::memcpy(img + h.off_dequant_units, L.dequant.data(),
+                L.dequant.size() * sizeof(PkaDequantUnit));
 
   plan->params = *p;
   plan->hdr = h;
@@ -940,8 +984,31 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
     a.items = reinterpret_cast<const PkaWorkItem*>(plan->int_ws_d + h.off_prefill_items);
     // the Q (and ragged K/V) tensor maps span the buffers' declared rows
     const int rows = graph ? p->graph_max_qo_rows : plan->info.nnz_qo;
-    const int64_t kv_rows = graph ? p->graph_max_kv_tokens : plan->info.total_kv;
-    cudaError_t e = pka::launch_prefill(a, h.num_prefill_ctas, p->head_dim, g, rows, kv_rows,
+    int64_t kv_rows = graph ? p->graph_max_kv_tokens : plan->info.total_kv;
+    pka::AttnArgs pa = a;
+    if (h.num_dequant_units > 0) {
+      // e4m3 K/V: decode the keys of the tensor-core requests to bf16 in the
+      // float workspace (after the partial states); the tensor-core kernel
+      // then reads them as ragged K/V
+      const size_t rec_lse = plan->layout_records
+                                 ? (((size_t)plan->layout_records * 4 + 255) & ~size_t(255))
+                                 : 0;
+      char* base = static_cast<char*>(float_ws) + (plan->layout_records ? rec_o_al : 0) + rec_lse;
+      uint16_t* sk = reinterpret_cast<uint16_t*>(base);
+      uint16_t* sv = reinterpret_cast<uint16_t*>(base + kv_scratch_bytes(p, h.dequant_rows));
+      cudaError_t e = pka::launch_dequant(
+          reinterpret_cast<const PkaDequantUnit*>(plan->int_ws_d + h.off_dequant_units),
+          h.num_dequant_units, h.dequant_rows, kv_indices, k, v, page_stride, p->page_size,
+          p->layout, p->kv_ragged, p->num_kv_heads, p->head_dim, sk, sv, st);
+      if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
+      pa.k = sk;
+      pa.v = sv;
+      pa.kv_ragged = 1;
+      pa.page_size = 1;
+      pa.kv_fp8 = 0;
+      kv_rows = h.dequant_rows;
+    }
+    cudaError_t e = pka::launch_prefill(pa, h.num_prefill_ctas, p->head_dim, g, rows, kv_rows,
                                          &plan->prefill_maps, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }

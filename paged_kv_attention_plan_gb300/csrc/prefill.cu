@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- epilogue
       const bool store = i_tok < w.q_count;
       const bool any = l > 0.f;
-      const float inv = any ? 1.f / l : 0.f;
+      const float inv = any ? a.v_scale / l : 0.f;  // V's scale (1 for bf16 K/V)
       const int head = w.kv_head0 * G + g;
       uint16_t* odst = a.o + ((int64_t)(w.q_row0 + i_tok) * a.num_qo_heads + head) * D;
       const int rec = w.out_rec + i_tok * G + g;

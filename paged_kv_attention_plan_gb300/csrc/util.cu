@@ -1,5 +1,7 @@
 // Bandwidth kernels around the attention launches: the state merge,
 // append_paged_kv_cache, packbits, and the device error word.
+#include <cuda_fp16.h>
+
 #include <mutex>
 
 #include "pka_device.cuh"
@@ -237,6 +239,79 @@ __global__ void __launch_bounds__(256) append_kernel(
 
 // Grid of a grid-stride kernel: enough blocks for the work, at most 32 per
 // multiprocessor of the current device.
+// ---------------------------------------------------------------------------
+// e4m3 K/V for the tensor-core rows: decode the keys of each listed request
+// (logical position j -> page kv_indices[kv_base + j / P], slot j % P, the
+// addressing of "Causality uses logical positions, not page numbers"; ragged
+// K/V: row kv_base + j, "KV-Cache layouts", "Ragged Tensor") from
+// the e4m3 pools into bf16 rows dst_row0 + j of [rows, Hk, D] scratch
+// tensors.  e4m3 -> f16 is exact (cvt), and so is f16 -> f32 -> bf16 for
+// every e4m3 value; the pool scales are not applied here (K's is folded into
+// the softmax scale, V's into the output).  One thread converts 16 codes of
+// K and of V; the unit of a row comes from a binary search of dst_row0.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("{\n .reg .b16 c;\n cvt.u16.u32 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;\n}"
+      : "=r"(h2)
+      : "r"(two_codes));
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+  return float2_to_bf16x2(lo, hi);
+}
+
+__global__ void __launch_bounds__(256) dequant_kernel(
+    const PkaDequantUnit* __restrict__ units, int n_units, int64_t rows,
+    const int32_t* __restrict__ kv_indices, const uint8_t* __restrict__ k8,
+    const uint8_t* __restrict__ v8, int64_t page_stride, int P, int layout, int ragged, int hk,
+    int d, uint16_t* __restrict__ out_k, uint16_t* __restrict__ out_v) {
+  const int vec_per_head = d / 16;  // 16 codes per thread
+  const int64_t vec_per_row = (int64_t)hk * vec_per_head;
+  const int64_t total = rows * vec_per_row;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = x / vec_per_row;
+    const int rem = (int)(x - row * vec_per_row);
+    const int h = rem / vec_per_head;
+    const int c = rem - h * vec_per_head;
+    int lo = 0, hi = n_units - 1;  // last unit with dst_row0 <= row
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (units[mid].dst_row0 <= row) lo = mid; else hi = mid - 1;
+    }
+    const PkaDequantUnit u = units[lo];
+    const int j = (int)(row - u.dst_row0);
+    int64_t src;
+    if (ragged) {  // ragged K/V: key j of the request is row kv_base + j
+      src = ((int64_t)(u.kv_base + j) * hk + h) * d;
+    } else {
+      const int page = kv_indices[u.kv_base + j / P];
+      const int slot = j % P;
+      src = (int64_t)page * page_stride;
+      src += layout == PKA_NHD ? ((int64_t)slot * hk + h) * d : ((int64_t)h * P + slot) * d;
+    }
+    src += c * 16;
+    const int64_t dst = (row * hk + h) * d + c * 16;
+    const uint4 kc = *reinterpret_cast<const uint4*>(k8 + src);
+    const uint4 vc = *reinterpret_cast<const uint4*>(v8 + src);
+    const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w}, vw[4] = {vc.x, vc.y, vc.z, vc.w};
+    uint32_t ko[8], vo[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ko[2 * i] = e4m3x2_to_bf16x2(kw[i] & 0xffffu);
+      ko[2 * i + 1] = e4m3x2_to_bf16x2(kw[i] >> 16);
+      vo[2 * i] = e4m3x2_to_bf16x2(vw[i] & 0xffffu);
+      vo[2 * i + 1] = e4m3x2_to_bf16x2(vw[i] >> 16);
+    }
+    uint4* dk = reinterpret_cast<uint4*>(out_k + dst);
+    uint4* dv = reinterpret_cast<uint4*>(out_v + dst);
+    dk[0] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+    dk[1] = make_uint4(ko[4], ko[5], ko[6], ko[7]);
+    dv[0] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+    dv[1] = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+  }
+}
+
 // Self-test of the bounded barrier waits: warps 0 and 1 wait with the
 // warp-wide wait, lane 0 of warp 2 with the single-thread wait, all on one
 // mbarrier of count 1 and with `polls` polls.  With `arrive` set, lane 0 of
@@ -279,6 +354,19 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
     merge_kernel<128><<<blocks, 256, 0, stream>>>(a);
   else
     merge_kernel<64><<<blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const PkaDequantUnit* units, int n_units, int64_t rows,
+                           const int32_t* kv_indices, const void* k8, const void* v8,
+                           int64_t page_stride, int page_size, int layout, int ragged, int hk,
+                           int d, uint16_t* out_k, uint16_t* out_v, cudaStream_t stream) {
+  if (n_units <= 0 || rows <= 0) return cudaSuccess;
+  const int64_t work = rows * hk * (d / 16);
+  dequant_kernel<<<grid_for(work, 256), 256, 0, stream>>>(
+      units, n_units, rows, kv_indices, static_cast<const uint8_t*>(k8),
+      static_cast<const uint8_t*>(v8), page_stride, page_size, layout, ragged, hk, d, out_k,
+      out_v);
   return cudaGetLastError();
 }
 

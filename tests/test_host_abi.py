@@ -405,18 +405,36 @@ def test_append_rejects_misaligned_buffers_and_strides():
     assert call(bf, nnz=0) == OK  # nothing to append: no device work
 
 
-def test_fp8_kv_is_decode_only():
-    """e4m3 K/V pools are read by the decode kernel only: batches with rows of
-    qo_len >= 2 are refused."""
-    b = W.make_paged_batch(3, [1, 5, 1], [10, 20, 30], page_size=4, hq=8, hk=2, d=64,
+def test_fp8_kv_tensor_core_rows_plan_a_bf16_scratch():
+    """e4m3 K/V: rows with qo_len >= 2 are planned over a bf16 scratch of their
+    requests' keys (dequant units in the image, items reading scratch rows);
+    graph mode refuses them, decode-only batches need no scratch."""
+    b = W.make_paged_batch(3, [1, 5, 1, 3], [10, 20, 30, 7], page_size=4, hq=8, hk=2, d=64,
                            with_payload=False)
-    p = pka.make_params(8, 2, 64, 4, kv_dtype="e4m3")
-    assert pka.pka_validate(p, b.qo_indptr, b.kv_indptr, b.last_page_len) == UNSUPPORTED
+    p = pka.make_params(8, 2, 64, 4, kv_dtype="e4m3", num_sms=152)
+    assert pka.pka_validate(p, b.qo_indptr, b.kv_indptr, b.last_page_len) == OK
     h = pka.pka_plan_create()
     buf = np.zeros(1 << 20, np.uint8)
     assert pka.pka_plan(h, p, b.qo_indptr, b.kv_indptr, b.last_page_len, None, buf,
-                        check=False) == UNSUPPORTED
+                        check=False) == OK
+    info = pka.pka_plan_get_info(h)
+    assert info.kv_scratch_rows == 20 + 7  # the two requests with qo_len >= 2
+    scratch = 2 * ((27 * 2 * 64 * 2 + 255) // 256 * 256)
+    assert info.float_ws_bytes >= scratch
+    img = parse(buf[: info.int_ws_bytes])
+    assert img["header"]["dequant_rows"] == 27
+    units = img["dequant_units"]
+    assert [u["kv_base"] for u in units] == [int(b.kv_indptr[1]), int(b.kv_indptr[3])]
+    assert [u["kv_len"] for u in units] == [20, 7] and [u["dst_row0"] for u in units] == [0, 20]
+    for it in img["prefill_items"]:
+        assert it["kv_base"] == (0 if it["req"] == 1 else 20)
+    for it in img["decode_items"]:
+        assert it["kv_base"] == int(b.kv_indptr[it["req"]])
     assert pka.pka_plan(h, p, None, b.kv_indptr, b.last_page_len, None, buf, check=False) == 0
+    assert pka.pka_plan_get_info(h).kv_scratch_rows == 0
+    g = pka.make_params(8, 2, 64, 4, kv_dtype="e4m3", graph_max_batch=8, graph_max_qo_rows=64)
+    assert pka.pka_plan(h, g, b.qo_indptr, b.kv_indptr, b.last_page_len, None, buf,
+                        check=False) == UNSUPPORTED
     pka.pka_plan_destroy(h)
     bad = pka.make_params(8, 2, 64, 4)
     bad.kv_dtype = 7

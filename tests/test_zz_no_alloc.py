@@ -96,8 +96,9 @@ def test_static_scratch_split_prefill_matches_oracle():
                            d=128)
     attn = pka.BatchAttention()
     info = attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, num_qo_heads=16, num_kv_heads=4,
-                     head_dim=128, page_size=16, split_mode="fixed", fixed_split_pages=5)
+                     head_dim=128, page_size=16, split_mode="fixed", fixed_split_pages=12)
     assert info.num_prefill_items > 0 and info.num_merge_tasks > 0
+    assert 0 < info.float_ws_bytes <= 16 << 20  # fits the static array
     o_ref, lse_ref = run_oracle(b)
     q, k, v, idx = bf16(b.q), bf16(b.k_pool), bf16(b.v_pool), i32(b.kv_indices)
     for _ in range(2):

@@ -2,6 +2,7 @@
 // append_paged_kv_cache, packbits, and the device error word.
 #include <cuda_fp16.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "pka_device.cuh"
@@ -170,20 +171,26 @@ __global__ void __launch_bounds__(256) packbits_kernel(const uint8_t* __restrict
 // ---------------------------------------------------------------------------
 // append_paged_kv_cache ("KV-Cache layouts", "Page table layout"): appended
 // row t of request r goes to logical position kv_len - n_append + t, i.e.
-// page kv_indices[kv_indptr[r] + pos / P], slot pos % P.  One thread moves
-// 16 bytes of K and of V; the request of a row comes from a binary search of
-// append_indptr.
+// page kv_indices[kv_indptr[r] + pos / P], slot pos % P.  One warp per
+// appended row: the request (a binary search of append_indptr), page and
+// slot are warp-uniform, and the lanes move the row's Hk * D elements of K
+// and of V in 16-byte pieces (coalesced loads of the row; stores of whole
+// head rows, contiguous across heads in NHD pages).
 // ---------------------------------------------------------------------------
 // e4m3 pools: 8 values, each divided by the pool's scale (correctly rounded
 // float32 division), then rounded to nearest even e4m3 with saturation at the
 // largest finite value (cvt .satfinite), 8 codes packed little-endian.
-__device__ __forceinline__ uint2 bf16x8_to_e4m3x8(uint4 x, float scale) {
+// A power-of-two scale divides exactly by a multiplication with its
+// reciprocal (both give the correctly rounded x / scale), so `inv` > 0 takes
+// that path and inv == 0 the division.
+__device__ __forceinline__ uint2 bf16x8_to_e4m3x8(uint4 x, float scale, float inv) {
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
   uint32_t pk[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 f = bf16x2_to_float2(w[i]);
-    const float lo = __fdiv_rn(f.x, scale), hi = __fdiv_rn(f.y, scale);
+    const float lo = inv > 0.f ? f.x * inv : __fdiv_rn(f.x, scale);
+    const float hi = inv > 0.f ? f.y * inv : __fdiv_rn(f.y, scale);
     uint32_t r;
     asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n cvt.u32.u16 %0, t;\n}"
         : "=r"(r)
@@ -199,16 +206,16 @@ __global__ void __launch_bounds__(256) append_kernel(
     const int32_t* __restrict__ append_indptr, int32_t batch, int64_t nnz,
     const int32_t* __restrict__ kv_indptr, const int32_t* __restrict__ kv_indices,
     const int32_t* __restrict__ last_page_len, void* __restrict__ k, void* __restrict__ v,
-    int64_t page_stride, int hk, int d, int P, int layout, float k_scale, float v_scale) {
-  const int vec_per_head = d / 8;
-  const int64_t vec_per_row = (int64_t)hk * vec_per_head;
-  const int64_t total = nnz * vec_per_row;
-  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total;
-       x += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = x / vec_per_row;
-    const int rem = (int)(x - row * vec_per_row);
-    const int h = rem / vec_per_head;
-    const int c = rem - h * vec_per_head;
+    int64_t page_stride, int hk, int d, int P, int layout, float k_scale, float v_scale,
+    float k_inv, float v_inv) {
+  constexpr int U = 4;  // 16-byte pieces per lane in flight
+  const int lane = threadIdx.x & 31;
+  const int vsh = d == 128 ? 4 : 3;  // log2 of the 16-byte pieces of one head row
+  const int per_head = 1 << vsh;
+  const int per_row = hk * per_head;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); row < nnz;
+       row += nwarps) {
     int lo = 0, hi = batch - 1;  // last r with append_indptr[r] <= row
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -221,24 +228,42 @@ __global__ void __launch_bounds__(256) append_kernel(
     const int pos = kv_len - n_app + (int)(row - append_indptr[r]);
     const int page = kv_indices[kv_indptr[r] + pos / P];
     const int slot = pos % P;
-    int64_t dst = (int64_t)page * page_stride;
-    dst += layout == PKA_NHD ? ((int64_t)slot * hk + h) * d : ((int64_t)h * P + slot) * d;
-    dst += c * 8;
-    const int64_t src = (row * hk + h) * d + c * 8;
-    const uint4 kx = *reinterpret_cast<const uint4*>(k_new + src);
-    const uint4 vx = *reinterpret_cast<const uint4*>(v_new + src);
-    if constexpr (F8) {  // element offsets are byte offsets in e4m3 pools
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(k) + dst) = bf16x8_to_e4m3x8(kx, k_scale);
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(v) + dst) = bf16x8_to_e4m3x8(vx, v_scale);
-    } else {
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(k) + dst) = kx;
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(v) + dst) = vx;
+    const int64_t page_off = (int64_t)page * page_stride;
+    const uint4* ks = reinterpret_cast<const uint4*>(k_new + row * (int64_t)per_row * 8);
+    const uint4* vs = reinterpret_cast<const uint4*>(v_new + row * (int64_t)per_row * 8);
+    for (int c0 = lane; c0 < per_row; c0 += 32 * U) {
+      uint4 kx[U], vx[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < per_row) {
+          kx[u] = ks[c];
+          vx[u] = vs[c];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= per_row) continue;
+        const int h = c >> vsh, cc = c & (per_head - 1);
+        const int64_t dst = page_off +
+                            (layout == PKA_NHD ? ((int64_t)slot * hk + h) * d
+                                               : ((int64_t)h * P + slot) * d) +
+                            cc * 8;
+        if constexpr (F8) {  // element offsets are byte offsets in e4m3 pools
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(k) + dst) =
+              bf16x8_to_e4m3x8(kx[u], k_scale, k_inv);
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(v) + dst) =
+              bf16x8_to_e4m3x8(vx[u], v_scale, v_inv);
+        } else {
+          *reinterpret_cast<uint4*>(static_cast<uint16_t*>(k) + dst) = kx[u];
+          *reinterpret_cast<uint4*>(static_cast<uint16_t*>(v) + dst) = vx[u];
+        }
+      }
     }
   }
 }
 
-// Grid of a grid-stride kernel: enough blocks for the work, at most 32 per
-// multiprocessor of the current device.
 // ---------------------------------------------------------------------------
 // e4m3 K/V for the tensor-core rows: decode the keys of each listed request
 // (logical position j -> page kv_indices[kv_base + j / P], slot j % P, the
@@ -336,6 +361,8 @@ __global__ void __launch_bounds__(96) wait_selftest_kernel(int arrive, uint32_t 
   if (!ok && err) atomicExch(err, (int32_t)PKA_ERR_DEVICE_TIMEOUT);
 }
 
+// Grid of a grid-stride kernel: enough blocks for the work, at most 32 per
+// multiprocessor of the current device.
 int grid_for(int64_t work, int block) {
   int64_t g = (work + block - 1) / block;
   int sms = current_device_sms();
@@ -385,16 +412,22 @@ cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_
                           const int32_t* kv_indptr, const int32_t* kv_indices,
                           const int32_t* last_page_len, void* k, void* v,
                           int64_t page_stride, cudaStream_t stream) {
-  const int64_t work = nnz * p.num_kv_heads * (p.head_dim / 8);
+  const int64_t threads = nnz * 32;  // one warp per appended row
   const float ks = p.k_scale > 0.f ? p.k_scale : 1.f, vs = p.v_scale > 0.f ? p.v_scale : 1.f;
+  // reciprocal of a power-of-two scale (exact), else 0: divide
+  auto pow2_inv = [](float s) {
+    int e = 0;
+    return std::frexp(s, &e) == 0.5f ? std::ldexp(1.0f, 1 - e) : 0.f;
+  };
   if (p.kv_dtype == PKA_KV_FP8_E4M3)
-    append_kernel<true><<<grid_for(work, 256), 256, 0, stream>>>(
+    append_kernel<true><<<grid_for(threads, 256), 256, 0, stream>>>(
         k_new, v_new, append_indptr, batch, nnz, kv_indptr, kv_indices, last_page_len, k, v,
-        page_stride, p.num_kv_heads, p.head_dim, p.page_size, p.layout, ks, vs);
+        page_stride, p.num_kv_heads, p.head_dim, p.page_size, p.layout, ks, vs, pow2_inv(ks),
+        pow2_inv(vs));
   else
-    append_kernel<false><<<grid_for(work, 256), 256, 0, stream>>>(
+    append_kernel<false><<<grid_for(threads, 256), 256, 0, stream>>>(
         k_new, v_new, append_indptr, batch, nnz, kv_indptr, kv_indices, last_page_len, k, v,
-        page_stride, p.num_kv_heads, p.head_dim, p.page_size, p.layout, 1.f, 1.f);
+        page_stride, p.num_kv_heads, p.head_dim, p.page_size, p.layout, 1.f, 1.f, 1.f, 1.f);
   return cudaGetLastError();
 }
 

@@ -271,12 +271,14 @@ class Cascade:
 
 
 def make_cascade_batch(seed, qo_lens, own_kv_lens, shared, *, page_size, layout=NHD, hq=32,
-                       hk=8, d=128, mask_mode="causal", with_payload=True, name="cascade"):
+                       hk=8, d=128, mask_mode="causal", with_payload=True, name="cascade",
+                       kv_dtype="bf16"):
     """Cascade over requests with query lengths ``qo_lens`` and own (last-level)
     KV lengths ``own_kv_lens``.  ``shared`` lists the levels above the last,
     root first; each is a list of (requests, kv_len) nodes that partition the
     requests in order.  Page ids are a seeded permutation of a pool with
-    exactly the pages needed, consumed level by level; unused slots hold NaN."""
+    exactly the pages needed, consumed level by level; unused slots hold NaN
+    (bf16 bits, or the e4m3 NaN code for kv_dtype "e4m3")."""
     rng = np.random.default_rng(seed)
     qo_lens = np.asarray(qo_lens, dtype=np.int64)
     q_ptr = _prefix(qo_lens)
@@ -305,8 +307,12 @@ def make_cascade_batch(seed, qo_lens, own_kv_lens, shared, *, page_size, layout=
     if with_payload:
         c.q = normal_bf16_bits(rng, (int(q_ptr[-1]), hq, d))
         shape = (total, page_size, hk, d) if layout == NHD else (total, hk, page_size, d)
-        c.k_pool = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
-        c.v_pool = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
+        if kv_dtype == "e4m3":
+            c.k_pool = np.full(shape, E4M3_NAN_CODE, dtype=np.uint8)
+            c.v_pool = np.full(shape, E4M3_NAN_CODE, dtype=np.uint8)
+        else:
+            c.k_pool = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
+            c.v_pool = np.full(shape, BF16_NAN_BITS, dtype=np.uint16)
         for lv in levels:
             fill_pages(rng, c.k_pool, c.v_pool, lv["kv_lens"], lv["kv_indptr"], lv["kv_indices"],
                        page_size, layout)

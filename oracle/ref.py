@@ -381,7 +381,8 @@ def _node_kv_len(level, n: int, page_size: int) -> int:
 
 
 def cascade_attention(q_bits, k_pool_bits, v_pool_bits, *, levels, page_size, num_qo_heads,
-                      num_kv_heads, layout="NHD", mask_mode="causal", sm_scale=None):
+                      num_kv_heads, layout="NHD", mask_mode="causal", sm_scale=None,
+                      kv_dtype="bf16", k_scale=1.0, v_scale=1.0):
     """Reference output of a multi-level cascade over one page pool.
 
     ``levels`` lists, from the root, dicts with the level's own qo_indptr,
@@ -392,7 +393,8 @@ def cascade_attention(q_bits, k_pool_bits, v_pool_bits, *, levels, page_size, nu
     the keys of its node that ``mask_mode`` leaves visible, with that node's
     (Q, K) and the row's index inside it.  The state is the softmax over the
     union of those key sets, taken in one pass: no merge.  A shared-level node
-    may hold no pages."""
+    may hold no pages.  ``kv_dtype`` "e4m3": the pool holds e4m3 codes read as
+    in batch_attention (code times the pool's scale)."""
     q = bf16_bits_to_f64(q_bits)
     nnz, _, head_dim = q.shape
     group = num_qo_heads // num_kv_heads
@@ -407,10 +409,10 @@ def cascade_attention(q_bits, k_pool_bits, v_pool_bits, *, levels, page_size, nu
         if (li, n) not in cache:
             lv = levels[li]
             klen = _node_kv_len(lv, n, page_size)
-            kv = [bf16_bits_to_f64(gather_request_kv(
+            kv = [kv_payload_to_f64(gather_request_kv(
                 pool, layout=layout, page_size=page_size, kv_indptr=lv["kv_indptr"],
-                kv_indices=lv["kv_indices"], req=n, kv_len=klen)) for pool in (k_pool_bits,
-                                                                               v_pool_bits)]
+                kv_indices=lv["kv_indices"], req=n, kv_len=klen), kv_dtype, scale_)
+                  for pool, scale_ in ((k_pool_bits, k_scale), (v_pool_bits, v_scale))]
             cache[(li, n)] = (klen, kv[0], kv[1])
         return cache[(li, n)]
 

@@ -135,3 +135,44 @@ def test_causal_at_a_shared_level_would_be_caught():
                                   (own[0][row, 0], own[1][row, 0])])
         assert np.allclose(om, o[row, 0], atol=1e-12)
         assert not np.allclose(own[0][row, 0], o[row, 0], atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# e4m3 pools: the same reading as flat attention (code times the pool scale)
+# ---------------------------------------------------------------------------
+
+def _bf16_copy(codes, scale):
+    vals = ref.e4m3_to_f64(codes) * scale
+    bits = (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    fin = ~np.isnan(vals)
+    assert np.array_equal(ref.bf16_bits_to_f64(bits)[fin], vals[fin])  # exact in bf16
+    return bits
+
+
+@pytest.mark.parametrize("layout,page_size", [("NHD", 4), ("HND", 16)])
+def test_fp8_cascade_equals_bf16_of_decoded_values(layout, page_size):
+    c = W.make_cascade_batch(41, [17, 1, 40, 3], [30, 5, 41, 3], [[(4, 300)], [(2, 64), (2, 20)]],
+                             page_size=page_size, layout=layout, hq=8, hk=2, d=64,
+                             kv_dtype="e4m3")
+    o8, l8 = _cascade(c, kv_dtype="e4m3", k_scale=0.5, v_scale=2.0)
+    c16 = W.make_cascade_batch(41, [17, 1, 40, 3], [30, 5, 41, 3],
+                               [[(4, 300)], [(2, 64), (2, 20)]], page_size=page_size,
+                               layout=layout, hq=8, hk=2, d=64, with_payload=False)
+    c16.q, c16.k_pool, c16.v_pool = c.q, _bf16_copy(c.k_pool, 0.5), _bf16_copy(c.v_pool, 2.0)
+    o16, l16 = _cascade(c16)
+    assert np.all(np.isfinite(o8))
+    assert np.allclose(o8, o16, rtol=0, atol=1e-12) and np.allclose(l8, l16, rtol=0, atol=1e-12)
+
+
+def test_fp8_cascade_equals_flat_page_tables():
+    # the shared node fills whole pages, so that the flat tables list every key once
+    c = W.make_cascade_batch(42, [9, 1, 1, 22], [12, 40, 7, 30], [[(4, 128)]], page_size=4,
+                             hq=8, hk=2, d=64, kv_dtype="e4m3")
+    o, lse = _cascade(c, kv_dtype="e4m3", k_scale=0.75, v_scale=1.5)
+    kv_indptr, kv_indices, last = _flat_tables(c)
+    qo = c.levels[-1]["qo_indptr"]
+    of, lf = ref.batch_attention(c.q, c.k_pool, c.v_pool, qo_indptr=qo, kv_indptr=kv_indptr,
+                                 kv_indices=kv_indices, last_page_len=last, page_size=4,
+                                 num_qo_heads=8, num_kv_heads=2, kv_dtype="e4m3", k_scale=0.75,
+                                 v_scale=1.5)
+    assert np.allclose(o, of, rtol=0, atol=1e-12) and np.allclose(lse, lf, rtol=0, atol=1e-12)

@@ -82,8 +82,9 @@ typedef enum pka_mask_mode {
  * elements = bytes) a multiple of 16.  Decode rows read the codes directly;
  * for rows with qo_len >= 2 (tensor cores) run() first decodes each such
  * request's keys to bf16 (exact) into a scratch in the float workspace
- * (info.kv_scratch_rows rows of K and of V), then reads that scratch.  Not
- * in graph mode or cascades for rows with qo_len >= 2. */
+ * (info.kv_scratch_rows rows of K and of V; in a cascade, each node's keys
+ * once), then reads that scratch.  Graph mode refuses e4m3 pools with rows of
+ * qo_len >= 2 (the scratch size depends on the batch). */
 typedef enum pka_kv_dtype { PKA_KV_BF16 = 0, PKA_KV_FP8_E4M3 = 1 } pka_kv_dtype;
 typedef enum pka_split_mode {
   PKA_SPLIT_OFF = 0,    /* one work item per (request, head block, q tile)   */
@@ -208,9 +209,9 @@ pka_status pka_plan(pka_plan_t plan, const pka_params* params, int32_t batch,
  *   after the sum of kv_indptr[l'][num_nodes[l']] over l' < l.  Each level's
  *   work writes fp32 partial states to the float workspace and the merge
  *   kernel combines every row's states into O and LSE in the same pka_run.
- *   Supported: paged K/V, mask none or causal, split off/auto/fixed, up to
- *   PKA_MAX_CASCADE_LEVELS levels; ragged K/V, custom masks and graph mode
- *   return PKA_ERR_UNSUPPORTED.  Workspace rules and errors as in pka_plan;
+ *   Supported: paged K/V (bf16 or e4m3 pools), mask none or causal, split
+ *   off/auto/fixed, up to PKA_MAX_CASCADE_LEVELS levels; ragged K/V, custom
+ *   masks and graph mode return PKA_ERR_UNSUPPORTED.  Workspace rules and errors as in pka_plan;
  *   rows split differently between levels give PKA_ERR_METADATA. */
 #define PKA_MAX_CASCADE_LEVELS 16
 pka_status pka_plan_cascade(pka_plan_t plan, const pka_params* params, int32_t num_levels,

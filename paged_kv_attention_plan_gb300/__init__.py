@@ -58,12 +58,14 @@ class BatchAttention:
 
     def plan_cascade(self, levels, *, num_qo_heads, num_kv_heads, head_dim, page_size=1,
                      layout="NHD", mask_mode="causal", sm_scale=0.0, split_mode="auto",
-                     fixed_split_pages=1, num_sms=0, stream=None):
+                     fixed_split_pages=1, num_sms=0, kv_dtype="bf16", k_scale=1.0, v_scale=1.0,
+                     stream=None):
         """Multi-level cascade: ``levels`` lists, root first, each level's
         (qo_indptr, kv_indptr, last_page_len); run() then takes the levels'
         page ids concatenated in level order as kv_indices."""
         params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, layout, mask_mode,
-                             sm_scale, False, split_mode, fixed_split_pages, num_sms)
+                             sm_scale, False, split_mode, fixed_split_pages, num_sms,
+                             kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale)
         return self._plan(params, "pka_plan_cascade", lambda: pka_plan_cascade(
             self.handle, params, levels, self.int_ws, self.pinned, stream, check=False))
 

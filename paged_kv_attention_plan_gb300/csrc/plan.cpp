@@ -12,6 +12,7 @@
 #include <cstddef>
 #include <cstdio>
 #include <cstring>
+#include <unordered_map>
 #include <vector>
 
 #include "pka_internal.h"
@@ -41,7 +42,7 @@ struct PlanLists {
   std::vector<int32_t> merge_slots;
   // e4m3 K/V: requests whose keys are decoded to bf16 for the tensor-core rows
   std::vector<PkaDequantUnit> dequant;
-  std::vector<int32_t> dequant_row0;  // per request: its first scratch row, or -1
+  std::unordered_map<int32_t, int32_t> dequant_row0;  // node page-list start -> first scratch row
   int64_t dequant_rows = 0;
 
   void reset(bool is_cascade) {
@@ -222,21 +223,22 @@ pka_status check_kv_dtype(const pka_params* p, const Batch& b) {
   return PKA_OK;
 }
 
-// e4m3 K/V: one dequant unit per request that tensor-core items read (in
-// request order, scratch rows back to back), and those items' kv_base
-// rewritten to the request's first scratch row (the kernel then reads the
-// scratch as ragged K/V).
-void plan_dequant(const std::vector<Batch>& lv, PlanLists* L) {
-  const Batch& b = lv[0];
-  L->dequant_row0.assign(b.kv_len.size(), -1);
-  for (const PkaWorkItem& w : L->pre_items) L->dequant_row0[w.req] = 0;
-  for (size_t r = 0; r < b.kv_len.size(); ++r) {
-    if (L->dequant_row0[r] < 0) continue;
-    L->dequant_row0[r] = (int32_t)L->dequant_rows;
-    L->dequant.push_back({b.kv_base[r], b.kv_len[r], (int32_t)L->dequant_rows, 0});
-    L->dequant_rows += b.kv_len[r];
+// e4m3 K/V: one dequant unit per request (or cascade node) that tensor-core
+// items read, identified by its page-list start kv_base (distinct for every
+// node with pages), its scratch rows back to back in the order the items meet
+// them; the items' kv_base is rewritten to the node's first scratch row (the
+// kernel then reads the scratch as ragged K/V).
+void plan_dequant(PlanLists* L) {
+  L->dequant_row0.clear();
+  for (PkaWorkItem& w : L->pre_items) {
+    auto it = L->dequant_row0.find(w.kv_base);
+    if (it == L->dequant_row0.end()) {
+      it = L->dequant_row0.emplace(w.kv_base, (int32_t)L->dequant_rows).first;
+      L->dequant.push_back({w.kv_base, w.kv_len, (int32_t)L->dequant_rows, 0});
+      L->dequant_rows += w.kv_len;
+    }
+    w.kv_base = it->second;
   }
-  for (PkaWorkItem& w : L->pre_items) w.kv_base = L->dequant_row0[w.req];
 }
 
 PkaWorkItem make_item(const Batch& b, int r, int kv_head0, int n_kv_heads, int q_local0,
@@ -657,7 +659,7 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   plan_decode(p, lv, num_sms, &L);
   plan_prefill(p, lv, num_sms, &L);
   if (cascade) build_slot_merges(&L, nnz, p->num_qo_heads);
-  if (p->kv_dtype == PKA_KV_FP8_E4M3 && !cascade && !L.pre_items.empty()) plan_dequant(lv, &L);
+  if (p->kv_dtype == PKA_KV_FP8_E4M3 && !L.pre_items.empty()) plan_dequant(&L);
   if (L.dequant_rows > INT32_MAX) return PKA_ERR_UNSUPPORTED;
   GraphCaps caps;
   if (graph) {
@@ -878,9 +880,7 @@ pka_status pka_plan_cascade(pka_plan_t plan, const pka_params* p, int32_t num_le
   plan->info = pka_plan_info{};
   pka_status s = check_supported(p);
   if (s != PKA_OK) return s;
-  if (p->kv_ragged || p->mask_mode == PKA_MASK_CUSTOM || graph_mode(p) ||
-      p->kv_dtype != PKA_KV_BF16)
-    return PKA_ERR_UNSUPPORTED;
+  if (p->kv_ragged || p->mask_mode == PKA_MASK_CUSTOM || graph_mode(p)) return PKA_ERR_UNSUPPORTED;
   if (num_levels < 1 || num_levels > PKA_MAX_CASCADE_LEVELS || !num_nodes || !qo || !kv || !last)
     return PKA_ERR_INVALID_ARG;
   std::vector<Batch> lv(num_levels);

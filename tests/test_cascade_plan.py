@@ -167,3 +167,24 @@ def test_cascade_rejections():
         assert s == INVALID
     finally:
         pka.pka_plan_destroy(h)
+
+
+def test_fp8_cascade_dequantizes_each_tensor_core_node_once():
+    """e4m3 pools: every node that tensor-core items read gets one dequant unit
+    (its page-list start and kv_len), and those items read its scratch rows."""
+    c = W.make_cascade_batch(5, [9, 1, 30, 3], [12, 40, 31, 3], [[(4, 257)], [(2, 64), (2, 20)]],
+                             page_size=4, hq=8, hk=2, d=64, with_payload=False)
+    p = pka.make_params(8, 2, 64, 4, kv_dtype="e4m3", num_sms=152)
+    h = pka.pka_plan_create()
+    buf = np.zeros(1 << 20, np.uint8)
+    levels = [(lv["qo_indptr"], lv["kv_indptr"], lv["last_page_len"]) for lv in c.levels]
+    assert pka.pka_plan_cascade(h, p, levels, None, buf, check=False) == 0
+    info = pka.pka_plan_get_info(h)
+    img = parse(buf[: info.int_ws_bytes])
+    units = img["dequant_units"]
+    assert len({u["kv_base"] for u in units}) == len(units)  # one unit per node
+    assert info.kv_scratch_rows == sum(u["kv_len"] for u in units) > 0
+    starts = {u["dst_row0"]: u for u in units}
+    for it in img["prefill_items"]:
+        assert it["kv_base"] in starts and starts[it["kv_base"]]["kv_len"] == it["kv_len"]
+    pka.pka_plan_destroy(h)

@@ -5,7 +5,8 @@ One plan holds the work of every level; each piece writes an fp32 partial
 state and the merge kernel combines each row's states from all levels in the
 same run().  Covers shared system prompts under decode rows, three-level
 trees with append rows and nodes without pages, page size 1 HND, no mask,
-and every split mode.
+and every split mode; the same trees over e4m3 pools (decode nodes read the
+codes, tensor-core nodes a bf16 scratch of each node's keys).
 """
 import numpy as np
 import pytest
@@ -14,7 +15,7 @@ import torch
 import paged_kv_attention_plan_gb300 as pka
 from oracle import ref
 from inputs import workloads as W
-from tests.gpu_util import assert_parity, bf16, f64, i32
+from tests.gpu_util import assert_parity, bf16, f64, i32, kv_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -84,3 +85,40 @@ def test_cascade_equals_flat_plan_of_the_same_tokens():
                         i32(np.asarray(kv_indices, np.int32)))
     torch.cuda.synchronize()
     assert_parity(o, lse, f64(o2), f64(lse2))
+
+
+FP8_CASES = {
+    "shared_prompt_decode": lambda: W.make_cascade_batch(
+        31, [1] * 32, np.random.default_rng(1).integers(1, 512, 32), [[(32, 2048)]],
+        page_size=16, layout="HND", hq=32, hk=8, d=128, kv_dtype="e4m3"),
+    "three_levels_append": lambda: W.make_cascade_batch(
+        32, [17, 1, 40, 3, 1, 9], [30, 5, 41, 3, 200, 9],
+        [[(6, 700)], [(2, 64), (1, 0), (3, 129)]], page_size=4, hq=16, hk=2, d=64,
+        kv_dtype="e4m3"),
+    "shared_prefix_prefill": lambda: W.make_cascade_batch(
+        33, [128] * 4, [128] * 4, [[(4, 1500)]], page_size=16, layout="HND", hq=32, hk=8,
+        d=128, kv_dtype="e4m3"),
+}
+
+
+@pytest.mark.parametrize("split", [("auto", 1), ("fixed", 3)])
+@pytest.mark.parametrize("case", list(FP8_CASES))
+def test_fp8_cascade_parity(case, split):
+    c = FP8_CASES[case]()
+    attn = pka.BatchAttention()
+    info = attn.plan_cascade(
+        [(lv["qo_indptr"], lv["kv_indptr"], lv["last_page_len"]) for lv in c.levels],
+        num_qo_heads=c.num_qo_heads, num_kv_heads=c.num_kv_heads, head_dim=c.head_dim,
+        page_size=c.page_size, layout=c.layout, mask_mode=c.mask_mode, split_mode=split[0],
+        fixed_split_pages=split[1], kv_dtype="e4m3", k_scale=0.5, v_scale=2.0)
+    o, lse = attn.run(bf16(c.q), kv_tensor(c.k_pool), kv_tensor(c.v_pool), i32(c.kv_indices))
+    torch.cuda.synchronize()
+    assert pka.pka_get_device_error() == 0
+    if info.num_prefill_items > 0:
+        assert info.kv_scratch_rows > 0
+    o_ref, lse_ref = ref.cascade_attention(c.q, c.k_pool, c.v_pool, levels=c.levels,
+                                           page_size=c.page_size, num_qo_heads=c.num_qo_heads,
+                                           num_kv_heads=c.num_kv_heads, layout=c.layout,
+                                           mask_mode=c.mask_mode, kv_dtype="e4m3", k_scale=0.5,
+                                           v_scale=2.0)
+    assert_parity(f64(o), f64(lse), o_ref, lse_ref)

@@ -214,17 +214,24 @@ def e2e_decode(d, steps, warmup, stream, device):
     pipelined as a serving loop runs them: step i+1's copies and plan() go on
     a copy stream while step i computes, and step i's result is read back on
     a third stream; device buffers and plans are double-buffered, ordered by
-    events, and all copies of all steps sit inside the timed region."""
+    events, and all copies of all steps sit inside the timed region.  Q and
+    kv_indices share one staging buffer (one copy in), O and LSE one output
+    buffer (one copy out)."""
     import paged_kv_attention_plan_gb300 as pka
     b = d["batch"]
-    q_h = d["q"].cpu().pin_memory()
-    idx_h = torch.from_numpy(b.kv_indices).pin_memory()
-    o_h = [torch.empty(d["o"].shape, dtype=d["o"].dtype).pin_memory() for _ in range(2)]
-    lse_h = [torch.empty(d["lse"].shape, dtype=torch.float32).pin_memory() for _ in range(2)]
-    q_d = [torch.empty_like(d["q"]) for _ in range(2)]
-    idx_d = [torch.empty_like(d["idx"]) for _ in range(2)]
-    o_d = [torch.empty_like(d["o"]) for _ in range(2)]
-    lse_d = [torch.empty_like(d["lse"]) for _ in range(2)]
+    q_bytes = d["q"].numel() * 2
+    idx_bytes = b.kv_indices.size * 4
+    o_bytes, lse_bytes = d["o"].numel() * 2, d["lse"].numel() * 4
+    in_h = torch.empty(q_bytes + idx_bytes, dtype=torch.uint8).pin_memory()
+    in_h[:q_bytes].view(torch.bfloat16).view(d["q"].shape).copy_(d["q"].cpu())
+    in_h[q_bytes:].view(torch.int32).copy_(torch.from_numpy(b.kv_indices))
+    out_h = [torch.empty(o_bytes + lse_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    in_d = [torch.empty(q_bytes + idx_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    out_d = [torch.empty(o_bytes + lse_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    q_d = [t[:q_bytes].view(torch.bfloat16).view(d["q"].shape) for t in in_d]
+    idx_d = [t[q_bytes:].view(torch.int32) for t in in_d]
+    o_d = [t[:o_bytes].view(torch.bfloat16).view(d["o"].shape) for t in out_d]
+    lse_d = [t[o_bytes:].view(torch.float32).view(d["lse"].shape) for t in out_d]
     attn = [pka.BatchAttention(device=device) for _ in range(2)]
     h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev = lambda: torch.cuda.Event()  # noqa: E731
@@ -237,8 +244,7 @@ def e2e_decode(d, steps, warmup, stream, device):
         s = i & 1
         h2d_s.wait_event(done[s])  # step i-2 no longer reads slot s
         with torch.cuda.stream(h2d_s):
-            q_d[s].copy_(q_h, non_blocking=True)
-            idx_d[s].copy_(idx_h, non_blocking=True)
+            in_d[s].copy_(in_h, non_blocking=True)
             attn[s].plan(None, b.kv_indptr, b.last_page_len, stream=h2d_s, **kw)
         ready[s].record(h2d_s)
         stream.wait_event(ready[s])
@@ -247,8 +253,7 @@ def e2e_decode(d, steps, warmup, stream, device):
         done[s].record(stream)
         d2h_s.wait_event(done[s])
         with torch.cuda.stream(d2h_s):
-            o_h[s].copy_(o_d[s], non_blocking=True)
-            lse_h[s].copy_(lse_d[s], non_blocking=True)
+            out_h[s].copy_(out_d[s], non_blocking=True)
         read[s].record(d2h_s)
 
     for i in range(warmup):
@@ -264,12 +269,19 @@ def e2e_decode(d, steps, warmup, stream, device):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     ms = max(ev0.elapsed_time(ev1), wall * 1e3) / steps
-    h2d = q_h.numel() * 2 + idx_h.numel() * 4 + int(attn[0].info.int_ws_bytes)
-    d2h = o_h[0].numel() * 2 + lse_h[0].numel() * 4
+    h2d = q_bytes + idx_bytes + int(attn[0].info.int_ws_bytes)
+    d2h = o_bytes + lse_bytes
+    # the last step's read-back against an output of the device-only loop
+    decode_step(d)
+    torch.cuda.synchronize()
+    o_last = out_h[(steps - 1) & 1][:o_bytes].view(torch.bfloat16).view(d["o"].shape).float()
+    diff = float((o_last - d["o"].cpu().float()).abs().max())
     return {"value": d["bytes"] / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "pipeline": "copies + plan on a copy stream, run on the compute stream, read-back "
-                        "on a third; double-buffered, all inside the timed region"}
+            "max_abs_diff_vs_device_loop": diff,
+            "pipeline": "Q + kv_indices copied in (one copy) and plan() on a copy stream, run on the "
+                        "compute stream, O + LSE read back (one copy) on a third; double-buffered, "
+                        "all inside the timed region"}
 
 
 def prefill_flops(b):

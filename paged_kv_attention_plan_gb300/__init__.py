@@ -36,6 +36,8 @@ class BatchAttention:
         self.float_ws = torch.empty(float_ws_bytes, dtype=torch.uint8, device=self.device)
         self.params = None
         self.info = None
+        self._params_key = None
+        self._params_cached = None
 
     def __del__(self):
         try:
@@ -48,10 +50,14 @@ class BatchAttention:
              split_mode="auto", fixed_split_pages=1, num_sms=0, graph_max_batch=0,
              graph_max_qo_rows=0, graph_max_kv_tokens=0, kv_dtype="bf16", k_scale=1.0,
              v_scale=1.0, decode_on_tensor_cores=False, stream=None):
-        params = make_params(num_qo_heads, num_kv_heads, head_dim, page_size, layout, mask_mode,
-                             sm_scale, kv_ragged, split_mode, fixed_split_pages, num_sms,
-                             graph_max_batch, graph_max_qo_rows, graph_max_kv_tokens, kv_dtype,
-                             k_scale, v_scale, decode_on_tensor_cores)
+        key = (num_qo_heads, num_kv_heads, head_dim, page_size, layout, mask_mode, sm_scale,
+               kv_ragged, split_mode, fixed_split_pages, num_sms, graph_max_batch,
+               graph_max_qo_rows, graph_max_kv_tokens, kv_dtype, k_scale, v_scale,
+               decode_on_tensor_cores)
+        if key != self._params_key:  # the same parameters plan after plan: build them once
+            self._params_cached = make_params(*key)
+            self._params_key = key
+        params = self._params_cached
         return self._plan(params, "pka_plan", lambda: pka_plan(
             self.handle, params, qo_indptr, kv_indptr, last_page_len, self.int_ws, self.pinned,
             stream, check=False))

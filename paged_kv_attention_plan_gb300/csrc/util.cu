@@ -66,7 +66,11 @@ namespace {
 // weight each state by 2^(b - shift), normalise the weights before the
 // weighted sum, and return shift + log2(sum of weights).  States with
 // b = -inf (no visible key) carry no weight; if every state is empty the
-// result is a zero vector and -inf.  One warp per (row, head).
+// result is a zero vector and -inf.  One warp per (row, head): lane k takes
+// the statistics of slots k, k + 32, ... (warp reductions for the shift and
+// the sum of weights; the first 32 slots' records and statistics stay in
+// registers), then the warp adds the weighted rows slot by slot in slot
+// order, eight rows in flight.
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void merge_one(const MergeArgs& a, const int task, const int lane) {
@@ -88,34 +92,76 @@ __device__ __forceinline__ void merge_one(const MergeArgs& a, const int task, co
     stride = a.heads;
   }
   // record of slot k: strided, or listed (stride 0)
-  auto rec_of = [&](int k) -> int64_t {
-    return stride ? (int64_t)rec_first + (int64_t)k * stride : (int64_t)a.slots[rec_first + k];
+  auto rec_of = [&](int k) -> int {
+    return stride ? rec_first + k * stride : a.slots[rec_first + k];
   };
-  float shift = -INFINITY;
-  for (int k = 0; k < nslots; ++k) shift = fmaxf(shift, a.part_lse[rec_of(k)]);
+  // slot `lane` (the first 32 slots) stays in registers for all three steps
+  int rec0 = 0;
+  float b0 = -INFINITY;
+  if (lane < nslots) {
+    rec0 = rec_of(lane);
+    b0 = a.part_lse[rec0];
+  }
+  float shift = b0;
+  for (int k = lane + 32; k < nslots; k += 32) shift = fmaxf(shift, a.part_lse[rec_of(k)]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    shift = fmaxf(shift, __shfl_xor_sync(0xffffffffu, shift, off));
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float z = 0.f;
   if (shift != -INFINITY) {
-    for (int k = 0; k < nslots; ++k) z += exp2f(a.part_lse[rec_of(k)] - shift);
+    z = exp2f(b0 - shift);  // 0 for an empty or absent slot
+    for (int k = lane + 32; k < nslots; k += 32) z += exp2f(a.part_lse[rec_of(k)] - shift);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     const float inv_z = 1.f / z;
-    for (int k = 0; k < nslots; ++k) {
-      const int64_t rec = rec_of(k);
-      const float b = a.part_lse[rec];
-      if (b == -INFINITY) continue;
-      const float scale = exp2f(b - shift) * inv_z;
-      const float* src = a.part_o + rec * D + lane * PER;
-      if constexpr (PER == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] += scale * x.x;
-        acc[1] += scale * x.y;
-        acc[2] += scale * x.z;
-        acc[3] += scale * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        acc[0] += scale * x.x;
-        acc[1] += scale * x.y;
+    constexpr int R = 8;  // rows in flight
+    for (int base = 0; base < nslots; base += 32) {
+      // this lane's slot of the chunk: its record and normalised weight
+      int rec = rec0;
+      float b = b0;
+      if (base > 0) {
+        rec = 0;
+        b = -INFINITY;
+        if (base + lane < nslots) {
+          rec = rec_of(base + lane);
+          b = a.part_lse[rec];
+        }
+      }
+      const float wgt = b == -INFINITY ? 0.f : exp2f(b - shift) * inv_z;
+      const int cnt = min(32, nslots - base);
+      for (int j = 0; j < cnt; j += R) {
+        float x[R][PER];
+        float wr[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+          wr[q] = __shfl_sync(0xffffffffu, wgt, (j + q) & 31);
+          const int r = __shfl_sync(0xffffffffu, rec, (j + q) & 31);
+          if (j + q < cnt && wr[q] != 0.f) {
+            const float* src = a.part_o + (int64_t)r * D + lane * PER;
+            if constexpr (PER == 4) {
+              const float4 v = *reinterpret_cast<const float4*>(src);
+              x[q][0] = v.x;
+              x[q][1] = v.y;
+              x[q][2] = v.z;
+              x[q][3] = v.w;
+            } else {
+              const float2 v = *reinterpret_cast<const float2*>(src);
+              x[q][0] = v.x;
+              x[q][1] = v.y;
+            }
+          } else {
+            wr[q] = 0.f;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) x[q][e] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] += wr[q] * x[q][e];
       }
     }
   }

@@ -382,7 +382,7 @@ def _node_kv_len(level, n: int, page_size: int) -> int:
 
 def cascade_attention(q_bits, k_pool_bits, v_pool_bits, *, levels, page_size, num_qo_heads,
                       num_kv_heads, layout="NHD", mask_mode="causal", sm_scale=None,
-                      kv_dtype="bf16", k_scale=1.0, v_scale=1.0):
+                      kv_dtype="bf16", k_scale=1.0, v_scale=1.0, rows=None):
     """Reference output of a multi-level cascade over one page pool.
 
     ``levels`` lists, from the root, dicts with the level's own qo_indptr,
@@ -394,7 +394,8 @@ def cascade_attention(q_bits, k_pool_bits, v_pool_bits, *, levels, page_size, nu
     (Q, K) and the row's index inside it.  The state is the softmax over the
     union of those key sets, taken in one pass: no merge.  A shared-level node
     may hold no pages.  ``kv_dtype`` "e4m3": the pool holds e4m3 codes read as
-    in batch_attention (code times the pool's scale)."""
+    in batch_attention (code times the pool's scale).  ``rows`` (a set of
+    query rows) computes only those rows; the others stay NaN."""
     q = bf16_bits_to_f64(q_bits)
     nnz, _, head_dim = q.shape
     group = num_qo_heads // num_kv_heads
@@ -416,9 +417,11 @@ def cascade_attention(q_bits, k_pool_bits, v_pool_bits, *, levels, page_size, nu
             cache[(li, n)] = (klen, kv[0], kv[1])
         return cache[(li, n)]
 
-    o = np.zeros(q.shape)
-    lse = np.zeros(q.shape[:2])
+    o = np.full(q.shape, np.nan)
+    lse = np.full(q.shape[:2], np.nan)
     for row in range(nnz):
+        if rows is not None and row not in rows:
+            continue
         ks, vs = [], []
         for li, lv in enumerate(levels):
             n = _node_of(lv["qo_indptr"], row)

@@ -122,3 +122,27 @@ def test_fp8_cascade_parity(case, split):
                                            mask_mode=c.mask_mode, kv_dtype="e4m3", k_scale=0.5,
                                            v_scale=2.0)
     assert_parity(f64(o), f64(lse), o_ref, lse_ref)
+
+
+def test_cascade_full_size_sampled_rows():
+    """The benchmark's cascade at full size (64 decode rows under a 32,768-token
+    shared prompt, own suffixes U[512, 2048], page 16, 32/8 heads, D 128) in
+    the plan the benchmark times: every root-level piece (the tensor-core
+    items, split over the CTAs) feeds every row, so the sampled rows check all
+    of them through the merge, together with the own-level decode items of
+    those rows."""
+    c = W.shared_prompt_decode()
+    attn = pka.BatchAttention()
+    info = attn.plan_cascade(
+        [(lv["qo_indptr"], lv["kv_indptr"], lv["last_page_len"]) for lv in c.levels],
+        num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    assert info.num_prefill_items > 1 and info.num_decode_items > 0
+    o, lse = attn.run(bf16(c.q), bf16(c.k_pool), bf16(c.v_pool), i32(c.kv_indices))
+    torch.cuda.synchronize()
+    assert pka.pka_get_device_error() == 0
+    rng = np.random.default_rng(5)
+    rows = {0, c.nnz_q - 1} | {int(r) for r in rng.choice(c.nnz_q, 14, replace=False)}
+    o_ref, lse_ref = ref.cascade_attention(c.q, c.k_pool, c.v_pool, levels=c.levels,
+                                           page_size=16, num_qo_heads=32, num_kv_heads=8,
+                                           rows=rows)
+    assert_parity(f64(o), f64(lse), o_ref, lse_ref, rows=rows)

@@ -9,17 +9,19 @@
 // j <= K - Q + i of "Causality uses logical positions, not page numbers", or
 // the packed custom mask of "KV-Cache layouts", "Mask layout (2D Ragged
 // Tensor)") -> online softmax in fp32 registers, one row per thread -> P
-// (bf16, shared memory) -> O += P V (tcgen05, fp32 in TMEM).  The epilogue
-// writes bf16 O and the base-2 LSE, or a normalised fp32 partial state that
-// the merge kernel combines ("A worked split-KV example").
+// (bf16, in tensor memory) -> O += P V (tcgen05, fp32 in TMEM).  The
+// epilogue writes bf16 O and the base-2 LSE, or a normalised fp32 partial
+// state that the merge kernel combines ("A worked split-KV example").
 //
 // Warp roles (352 threads): warpgroups 0 and 1 run the softmax and epilogue
 // of two 128-row query tiles of the same (request, kv head) (thread = row =
-// TMEM lane); warp 8 loads Q and the K ring, warp 10 the V ring (TMA for
-// whole pages, cp.async for the rest), warp 9 allocates TMEM and issues the
-// MMAs (the whole warp runs the issue loop; one elected lane issues).  Both query tiles share each K/V tile and the tensor core alternates
-// between them, so one tile's MMAs overlap the other tile's softmax.  P stays in tensor memory (it overwrites the first
-// half of its S tile) and feeds the P V product as the A operand.
+// TMEM lane); warp 8 loads Q and the K ring, warp 10 the V ring (TMA page
+// boxes and gather4 rows, cp.async for the rest), warp 9 allocates TMEM and
+// issues the MMAs (the whole warp runs the issue loop; one elected lane
+// issues).  Both query tiles share each K/V tile and the tensor core
+// alternates between them, so one tile's MMAs overlap the other tile's
+// softmax.  P stays in tensor memory (it overwrites the first half of its S
+// tile) and feeds the P V product as the A operand.
 #include <cudaTypedefs.h>
 
 #include <cmath>

@@ -83,8 +83,11 @@ typedef enum pka_mask_mode {
  * for rows with qo_len >= 2 (tensor cores) run() first decodes each such
  * request's keys to bf16 (exact) into a scratch in the float workspace
  * (info.kv_scratch_rows rows of K and of V; in a cascade, each node's keys
- * once), then reads that scratch.  Graph mode refuses e4m3 pools with rows of
- * qo_len >= 2 (the scratch size depends on the batch). */
+ * once), then reads that scratch.  In graph mode the scratch is laid out for
+ * graph_max_kv_tokens rows (the keys of all rows with qo_len >= 2 of any
+ * plan must fit); without that capacity graph mode refuses such rows
+ * (PKA_ERR_UNSUPPORTED), and a plan whose rows outgrow it gets
+ * PKA_ERR_WORKSPACE. */
 typedef enum pka_kv_dtype { PKA_KV_BF16 = 0, PKA_KV_FP8_E4M3 = 1 } pka_kv_dtype;
 typedef enum pka_split_mode {
   PKA_SPLIT_OFF = 0,    /* one work item per (request, head block, q tile)   */
@@ -112,7 +115,8 @@ typedef struct pka_params {
    * available in graph mode; prefill rows are not split. */
   int32_t graph_max_batch;     /* the most requests of any plan                */
   int32_t graph_max_qo_rows;   /* the most query rows; q and o hold this many   */
-  int32_t graph_max_kv_tokens; /* ragged K/V only: the most K/V rows            */
+  int32_t graph_max_kv_tokens; /* ragged K/V: the most K/V rows; e4m3 pools:    */
+                               /* the most keys of rows with qo_len >= 2       */
   int32_t kv_dtype;            /* pka_kv_dtype of the K/V pools                 */
   float k_scale;               /* PKA_KV_FP8_E4M3: scale of K codes (<= 0: 1)    */
   float v_scale;               /* PKA_KV_FP8_E4M3: scale of V codes (<= 0: 1)    */

@@ -112,6 +112,7 @@ cudaError_t launch_append(const pka_params& p, int32_t batch, const uint16_t* k_
                           int64_t page_stride, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int arrive, int polls, cudaStream_t stream);
 cudaError_t launch_dequant(const PkaDequantUnit* units, int n_units, int64_t rows,
+                           const int32_t* counts,
                            const int32_t* kv_indices, const void* k8, const void* v8,
                            int64_t page_stride, int page_size, int layout, int ragged, int hk,
                            int d, uint16_t* out_k, uint16_t* out_v, cudaStream_t stream);

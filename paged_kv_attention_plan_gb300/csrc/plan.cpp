@@ -76,6 +76,8 @@ struct pka_plan_s {
   int device = -1;
   int32_t layout_records = 0;  // partial records the float workspace is laid out for
   int32_t merge_capacity = 0;  // graph mode: merge tasks the image has room for
+  int32_t dequant_capacity = 0;      // graph mode: dequant units the image has room for
+  int64_t scratch_capacity = 0;      // rows the float workspace's bf16 K/V scratch is laid out for
   PlanLists lists;             // the planner's lists, reused by every plan
   pka::MapCache decode_maps{};   // tensor maps of the last run's launches
   pka::MapCache prefill_maps{};
@@ -136,6 +138,7 @@ bool graph_mode(const pka_params* p) { return p->graph_max_batch > 0; }
 // (request, kv head, query tile) and sum_r ceil(Q_r / tq) <= ceil(R / tq) + B.
 struct GraphCaps {
   int64_t dec_items = 0, pre_items = 0, merges = 0, records = 0, joins = 0;
+  int64_t dequant_units = 0, dequant_rows = 0;  // e4m3 K/V: bf16 scratch of tensor-core rows
 };
 
 GraphCaps graph_caps(const pka_params* p, int num_sms) {
@@ -151,6 +154,12 @@ GraphCaps graph_caps(const pka_params* p, int num_sms) {
     // split (request, kv head)); no merge tasks are left for the merge kernel
     c.joins = B * p->num_kv_heads;
     c.records = c.dec_items * hpc * g;
+  }
+  if (p->kv_dtype == PKA_KV_FP8_E4M3 && p->graph_max_kv_tokens > 0) {
+    // one unit per request with qo_len >= 2; its keys count against the
+    // declared K/V token capacity
+    c.dequant_units = B;
+    c.dequant_rows = p->graph_max_kv_tokens;
   }
   return c;
 }
@@ -214,12 +223,17 @@ pka_status derive(const pka_params* p, int32_t batch, const int32_t* qo, const i
 }
 
 // e4m3 K/V: decode rows read the codes; rows with qo_len >= 2 read a bf16
-// scratch decoded in run(), whose size depends on the batch, so graph mode
-// (fixed workspaces) refuses them.
+// scratch decoded in run(), whose size depends on the batch: graph mode
+// (fixed workspaces) sizes it by graph_max_kv_tokens and refuses such rows
+// when that capacity is not declared.
 pka_status check_kv_dtype(const pka_params* p, const Batch& b) {
-  if (p->kv_dtype != PKA_KV_FP8_E4M3 || !graph_mode(p)) return PKA_OK;
+  if (p->kv_dtype != PKA_KV_FP8_E4M3 || !graph_mode(p) || p->graph_max_kv_tokens > 0)
+    return PKA_OK;
   for (int32_t q : b.qo_len)
-    if (q >= 2) return PKA_ERR_UNSUPPORTED;
+    if (q >= 2) {
+      pka::set_last_error("graph mode over e4m3 pools with qo_len >= 2 rows needs graph_max_kv_tokens");
+      return PKA_ERR_UNSUPPORTED;
+    }
   return PKA_OK;
 }
 
@@ -668,7 +682,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
     fold_ctas(L.pre_cta_ptr, L.pre_items, num_sms);
     if ((int64_t)L.dec_items.size() > caps.dec_items ||
         (int64_t)L.pre_items.size() > caps.pre_items || (int64_t)L.merges.size() > caps.merges ||
-        L.records > caps.records || (int64_t)L.joins.size() > caps.joins) {
+        L.records > caps.records || (int64_t)L.joins.size() > caps.joins ||
+        (int64_t)L.dequant.size() > caps.dequant_units || L.dequant_rows > caps.dequant_rows) {
       pka::set_last_error("plan outgrew the graph-mode image capacities");
       return PKA_ERR_WORKSPACE;
     }
@@ -679,6 +694,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   const int64_t n_pre = graph ? caps.pre_items : (int64_t)L.pre_items.size();
   const int64_t n_merge = graph ? caps.merges : (int64_t)L.merges.size();
   const int64_t n_join = graph ? caps.joins : (int64_t)L.joins.size();
+  const int64_t n_dequant = graph ? caps.dequant_units : (int64_t)L.dequant.size();
+  const int64_t scratch_rows = graph ? caps.dequant_rows : L.dequant_rows;
   const int64_t layout_records = graph ? caps.records : L.records;
 
   PkaImageHeader h{};
@@ -712,9 +729,9 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   w = align_words(w + n_join * kJoinWords);
   constexpr size_t kDequantWords = sizeof(PkaDequantUnit) / 4;
   h.num_dequant_units = (int)L.dequant.size();
-  h.off_dequant_units = L.dequant.empty() ? 0 : (int)w;
+  h.off_dequant_units = n_dequant > 0 ? (int)w : 0;
   h.dequant_rows = (int)L.dequant_rows;
-  w = align_words(w + L.dequant.size() * kDequantWords);
+  w = align_words(w + n_dequant * kDequantWords);
   if (w > (size_t)INT32_MAX || layout_records > INT32_MAX / 256) {
     pka::set_last_error("plan image or partial records exceed 2^31");
     return PKA_ERR_UNSUPPORTED;
@@ -728,7 +745,7 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   info.float_ws_bytes =
       layout_records ? rec_o_al + (((size_t)layout_records * 4 + 255) & ~size_t(255)) : 0;
   // e4m3 K/V: the bf16 K and V scratch follow the partial states
-  info.float_ws_bytes += 2 * kv_scratch_bytes(p, L.dequant_rows);
+  info.float_ws_bytes += 2 * kv_scratch_bytes(p, scratch_rows);
   info.kv_scratch_rows = (int32_t)L.dequant_rows;
   info.num_requests = batch;
   info.nnz_qo = nnz;
@@ -761,6 +778,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
       ranges.push_back({(size_t)h.off_merge_tasks, L.merges.size() * kMergeWords});
     if (!L.joins.empty())
       ranges.push_back({(size_t)h.off_decode_joins, L.joins.size() * kJoinWords});
+    if (!L.dequant.empty())
+      ranges.push_back({(size_t)h.off_dequant_units, L.dequant.size() * kDequantWords});
   } else {
     ranges.push_back({0, w});
   }
@@ -788,6 +807,8 @@ pka_status plan_levels(pka_plan_t plan, const pka_params* p, const std::vector<B
   plan->int_ws_d = static_cast<int32_t*>(int_ws_d);
   plan->layout_records = (int32_t)layout_records;
   plan->merge_capacity = (int32_t)n_merge;
+  plan->dequant_capacity = (int32_t)n_dequant;
+  plan->scratch_capacity = scratch_rows;
   if (int_ws_d) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
@@ -986,27 +1007,32 @@ pka_status pka_run(pka_plan_t plan, const pka_params* p, const void* q, const vo
     const int rows = graph ? p->graph_max_qo_rows : plan->info.nnz_qo;
     int64_t kv_rows = graph ? p->graph_max_kv_tokens : plan->info.total_kv;
     pka::AttnArgs pa = a;
-    if (h.num_dequant_units > 0) {
+    if (graph ? plan->dequant_capacity > 0 : h.num_dequant_units > 0) {
       // e4m3 K/V: decode the keys of the tensor-core requests to bf16 in the
       // float workspace (after the partial states); the tensor-core kernel
-      // then reads them as ragged K/V
+      // then reads them as ragged K/V.  Graph mode lays the scratch out for
+      // its capacity and launches on that fixed size; the dequant kernel
+      // reads this plan's unit and row counts from the device image.
       const size_t rec_lse = plan->layout_records
                                  ? (((size_t)plan->layout_records * 4 + 255) & ~size_t(255))
                                  : 0;
       char* base = static_cast<char*>(float_ws) + (plan->layout_records ? rec_o_al : 0) + rec_lse;
       uint16_t* sk = reinterpret_cast<uint16_t*>(base);
-      uint16_t* sv = reinterpret_cast<uint16_t*>(base + kv_scratch_bytes(p, h.dequant_rows));
+      uint16_t* sv = reinterpret_cast<uint16_t*>(base + kv_scratch_bytes(p, plan->scratch_capacity));
+      const int32_t* counts =
+          graph ? plan->int_ws_d + offsetof(PkaImageHeader, num_dequant_units) / 4 : nullptr;
       cudaError_t e = pka::launch_dequant(
           reinterpret_cast<const PkaDequantUnit*>(plan->int_ws_d + h.off_dequant_units),
-          h.num_dequant_units, h.dequant_rows, kv_indices, k, v, page_stride, p->page_size,
-          p->layout, p->kv_ragged, p->num_kv_heads, p->head_dim, sk, sv, st);
+          graph ? plan->dequant_capacity : h.num_dequant_units,
+          graph ? plan->scratch_capacity : h.dequant_rows, counts, kv_indices, k, v, page_stride,
+          p->page_size, p->layout, p->kv_ragged, p->num_kv_heads, p->head_dim, sk, sv, st);
       if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
       pa.k = sk;
       pa.v = sv;
       pa.kv_ragged = 1;
       pa.page_size = 1;
       pa.kv_fp8 = 0;
-      kv_rows = h.dequant_rows;
+      kv_rows = plan->scratch_capacity;
     }
     cudaError_t e = pka::launch_prefill(pa, h.num_prefill_ctas, p->head_dim, g, rows, kv_rows,
                                          &plan->prefill_maps, st);

@@ -331,11 +331,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
   return float2_to_bf16x2(lo, hi);
 }
 
+// `counts` (graph mode): the plan's unit count and row count, read from the
+// device image (its num_dequant_units and dequant_rows words), bounded by the
+// capacities n_units and rows the launch was sized for.
 __global__ void __launch_bounds__(256) dequant_kernel(
     const PkaDequantUnit* __restrict__ units, int n_units, int64_t rows,
-    const int32_t* __restrict__ kv_indices, const uint8_t* __restrict__ k8,
-    const uint8_t* __restrict__ v8, int64_t page_stride, int P, int layout, int ragged, int hk,
-    int d, uint16_t* __restrict__ out_k, uint16_t* __restrict__ out_v) {
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ kv_indices,
+    const uint8_t* __restrict__ k8, const uint8_t* __restrict__ v8, int64_t page_stride, int P,
+    int layout, int ragged, int hk, int d, uint16_t* __restrict__ out_k,
+    uint16_t* __restrict__ out_v) {
+  if (counts) {
+    n_units = min(max(counts[0], 0), n_units);
+    rows = min((int64_t)max(counts[2], 0), rows);
+  }
+  if (n_units <= 0) return;
   const int vec_per_head = d / 16;  // 16 codes per thread
   const int64_t vec_per_row = (int64_t)hk * vec_per_head;
   const int64_t total = rows * vec_per_row;
@@ -431,13 +440,14 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_dequant(const PkaDequantUnit* units, int n_units, int64_t rows,
+                           const int32_t* counts,
                            const int32_t* kv_indices, const void* k8, const void* v8,
                            int64_t page_stride, int page_size, int layout, int ragged, int hk,
                            int d, uint16_t* out_k, uint16_t* out_v, cudaStream_t stream) {
   if (n_units <= 0 || rows <= 0) return cudaSuccess;
   const int64_t work = rows * hk * (d / 16);
   dequant_kernel<<<grid_for(work, 256), 256, 0, stream>>>(
-      units, n_units, rows, kv_indices, static_cast<const uint8_t*>(k8),
+      units, n_units, rows, counts, kv_indices, static_cast<const uint8_t*>(k8),
       static_cast<const uint8_t*>(v8), page_stride, page_size, layout, ragged, hk, d, out_k,
       out_v);
   return cudaGetLastError();

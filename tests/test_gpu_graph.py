@@ -11,7 +11,7 @@ import torch
 
 import paged_kv_attention_plan_gb300 as pka
 from inputs import workloads as W
-from tests.gpu_util import assert_parity, bf16, f64, i32, run_oracle
+from tests.gpu_util import assert_parity, bf16, f64, i32, kv_tensor, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -167,3 +167,66 @@ def test_graph_mode_ragged_custom_mask():
         assert pka.pka_get_device_error() == 0
         n = b.nnz_q
         assert_parity(f64(o_buf[:n]), f64(lse_buf[:n]), *run_oracle(b, packed_mask=packed))
+
+
+def test_graph_mode_e4m3_capture_serves_new_plans():
+    """Graph mode over e4m3 pools with rows of qo_len >= 2: the bf16 scratch
+    is laid out for graph_max_kv_tokens rows, the dequant kernel reads each
+    plan's unit and row counts from the device image, and one captured run()
+    serves plans with and without tensor-core rows."""
+    hq, hk, d, page_size = 32, 8, 128, 16
+    max_batch, max_rows, max_tc_keys = 8, 640, 12000
+    specs = PAGED_SPECS
+    pool_pages = (20000 + page_size - 1) // page_size + 8 * 2
+    # V's scale stays 1: rows that see one or two keys (kv_len 2, 17) output a V
+    # row itself, and with V's scale at 2 such values reach 7.5, where one bf16
+    # step of the output is 2^-5 and rounding alone nears the 2e-2 bound
+    batches = [W.make_paged_batch(70 + i, qo, kv, page_size=page_size, layout="HND", hq=hq,
+                                  hk=hk, d=d, pool_pages=pool_pages, kv_dtype="e4m3",
+                                  k_scale=0.5, v_scale=1.0)
+               for i, (qo, kv) in enumerate(specs)]
+    shape = batches[0].k_pool.shape
+    q_buf = torch.zeros(max_rows, hq, d, dtype=torch.bfloat16, device="cuda")
+    o_buf = torch.zeros_like(q_buf)
+    lse_buf = torch.zeros(max_rows, hq, dtype=torch.float32, device="cuda")
+    k_buf = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+    v_buf = torch.zeros_like(k_buf)
+    idx_buf = torch.zeros(pool_pages, dtype=torch.int32, device="cuda")
+    attn = pka.BatchAttention()
+    stream = torch.cuda.Stream()
+    kw = dict(num_qo_heads=hq, num_kv_heads=hk, head_dim=d, page_size=page_size, layout="HND",
+              graph_max_batch=max_batch, graph_max_qo_rows=max_rows,
+              graph_max_kv_tokens=max_tc_keys, kv_dtype="e4m3", k_scale=0.5, v_scale=1.0,
+              stream=stream)
+
+    def load(b):
+        q_buf[:b.nnz_q].copy_(bf16(b.q))
+        k_buf.copy_(kv_tensor(b.k_pool))
+        v_buf.copy_(kv_tensor(b.v_pool))
+        idx_buf[:len(b.kv_indices)].copy_(i32(b.kv_indices))
+        torch.cuda.synchronize()
+        return attn.plan(b.qo_indptr, b.kv_indptr, b.last_page_len, **kw)
+
+    def call():
+        attn.run(q_buf, k_buf, v_buf, idx_buf, out=o_buf, lse=lse_buf, stream=stream)
+
+    info = load(batches[0])
+    assert info.kv_scratch_rows > 0
+    with torch.cuda.stream(stream):
+        call()  # first call outside capture (one-time set-up)
+    torch.cuda.synchronize()
+    ws = (attn.int_ws.data_ptr(), attn.float_ws.data_ptr())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+    torch.cuda.synchronize()
+    for b in batches[1:] + batches[:1]:
+        load(b)
+        assert (attn.int_ws.data_ptr(), attn.float_ws.data_ptr()) == ws
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert pka.pka_get_device_error() == 0
+        n = b.nnz_q
+        assert_parity(f64(o_buf[:n]), f64(lse_buf[:n]), *run_oracle(b))

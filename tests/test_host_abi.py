@@ -408,7 +408,8 @@ def test_append_rejects_misaligned_buffers_and_strides():
 def test_fp8_kv_tensor_core_rows_plan_a_bf16_scratch():
     """e4m3 K/V: rows with qo_len >= 2 are planned over a bf16 scratch of their
     requests' keys (dequant units in the image, items reading scratch rows);
-    graph mode refuses them, decode-only batches need no scratch."""
+    graph mode needs graph_max_kv_tokens for them and then keeps one layout
+    (scratch laid out for the capacity), decode-only batches need no scratch."""
     b = W.make_paged_batch(3, [1, 5, 1, 3], [10, 20, 30, 7], page_size=4, hq=8, hk=2, d=64,
                            with_payload=False)
     p = pka.make_params(8, 2, 64, 4, kv_dtype="e4m3", num_sms=152)
@@ -434,7 +435,27 @@ def test_fp8_kv_tensor_core_rows_plan_a_bf16_scratch():
     assert pka.pka_plan_get_info(h).kv_scratch_rows == 0
     g = pka.make_params(8, 2, 64, 4, kv_dtype="e4m3", graph_max_batch=8, graph_max_qo_rows=64)
     assert pka.pka_plan(h, g, b.qo_indptr, b.kv_indptr, b.last_page_len, None, buf,
-                        check=False) == UNSUPPORTED
+                        check=False) == UNSUPPORTED  # no scratch capacity declared
+    # graph mode with a declared capacity: one fixed layout, scratch laid out for it
+    g = pka.make_params(8, 2, 64, 4, kv_dtype="e4m3", graph_max_batch=8, graph_max_qo_rows=64,
+                        graph_max_kv_tokens=100, num_sms=152)
+    layouts = []
+    for qo, kv in (([1, 5, 1, 3], [10, 20, 30, 7]), ([2, 1], [60, 9]), ([1, 1, 1], [4, 5, 6])):
+        c = W.make_paged_batch(4, qo, kv, page_size=4, hq=8, hk=2, d=64, with_payload=False)
+        buf[:] = 0
+        assert pka.pka_plan(h, g, c.qo_indptr, c.kv_indptr, c.last_page_len, None, buf,
+                            check=False) == OK
+        gi = pka.pka_plan_get_info(h)
+        hdr = parse(buf[: gi.int_ws_bytes])["header"]
+        tc = [k for q, k in zip(qo, kv) if q >= 2]
+        assert hdr["dequant_rows"] == sum(tc) and hdr["num_dequant_units"] == len(tc)
+        layouts.append((gi.int_ws_bytes, gi.float_ws_bytes, hdr["off_dequant_units"]))
+    assert len(set(layouts)) == 1 and layouts[0][2] > 0
+    assert layouts[0][1] >= 2 * ((100 * 2 * 64 * 2 + 255) // 256 * 256)
+    c = W.make_paged_batch(5, [3, 2], [70, 40], page_size=4, hq=8, hk=2, d=64,
+                           with_payload=False)
+    assert pka.pka_plan(h, g, c.qo_indptr, c.kv_indptr, c.last_page_len, None, buf,
+                        check=False) == WORKSPACE  # 110 keys > the 100-row scratch
     pka.pka_plan_destroy(h)
     bad = pka.make_params(8, 2, 64, 4)
     bad.kv_dtype = 7

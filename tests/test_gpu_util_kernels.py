@@ -117,7 +117,7 @@ def test_append_then_decode_e4m3():
 @pytest.mark.parametrize("dim", [64, 128])
 def test_merge_states_matches_oracle(dim):
     rng = np.random.default_rng(dim)
-    counts = [1, 2, 5, 0, 3, 7]
+    counts = [1, 2, 5, 0, 3, 7, 33, 70]  # rows past 32 states take further rounds of slots
     heads = 3
     indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     S = int(indptr[-1])
@@ -127,6 +127,11 @@ def test_merge_states_matches_oracle(dim):
     v[1, 0] = 0
     s[7:10, 1] = -np.inf  # a row whose states are all empty for head 1
     v[7:10, 1] = 0
+    r7 = int(indptr[7])
+    s[r7 + 40:r7 + 45, 2] = -np.inf  # empty states in the second round of slots
+    v[r7 + 40:r7 + 45, 2] = 0
+    s[r7 + 65, 0] = 30.0  # the largest statistic of a row in its third round
+
     v_out = torch.empty(len(counts), heads, dim, dtype=torch.bfloat16, device="cuda")
     s_out = torch.empty(len(counts), heads, dtype=torch.float32, device="cuda")
     pka.pka_merge_states(torch.from_numpy(v).cuda(), torch.from_numpy(s).cuda(), i32(indptr),

@@ -138,3 +138,27 @@ def test_graph_parameter_rules():
     r = SMALL["small_ragged"]()
     p = _params(r, max_batch=16, max_rows=512, max_kv=0)
     assert pka.pka_validate(p, r.qo_indptr, r.kv_indptr, r.last_page_len) == INVALID
+
+
+def test_graph_mode_e4m3_ragged_layout_is_fixed():
+    """Ragged e4m3 K/V in graph mode: graph_max_kv_tokens bounds both the
+    ragged rows and the bf16 scratch of the rows with qo_len >= 2, so the image
+    layout and the float workspace stay the same across batches, and each
+    plan's dequant units cover exactly its tensor-core requests."""
+    params = pka.make_params(16, 4, 64, 1, mask_mode="causal", kv_ragged=True, num_sms=SMS,
+                             graph_max_batch=6, graph_max_qo_rows=700, graph_max_kv_tokens=700,
+                             kv_dtype="e4m3")
+    layouts = []
+    for i, lens in enumerate([[300, 1, 200, 100], [1, 1, 1], [700], [64, 65, 1, 190, 2, 3]]):
+        b = W.make_ragged_batch(80 + i, lens, hq=16, hk=4, d=64, mask_mode="causal",
+                                with_payload=False)
+        s, info, buf = _plan(params, b)
+        assert s == OK, lens
+        img = parse(buf[: info.int_ws_bytes])
+        h = img["header"]
+        tc = [n for n in lens if n >= 2]
+        assert h["num_dequant_units"] == len(tc) and h["dequant_rows"] == sum(tc)
+        assert sorted(u["kv_len"] for u in img["dequant_units"]) == sorted(tc)  # in dealing order
+        layouts.append((info.int_ws_bytes, info.float_ws_bytes, h["off_dequant_units"],
+                        h["off_prefill_items"], h["num_prefill_ctas"]))
+    assert len(set(layouts)) == 1

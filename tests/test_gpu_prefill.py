@@ -4,8 +4,9 @@ Covers the worked three-request batch (printed and seeded page ids), the GPU
 smoke-check shape of "Deep Dive - FlashInfer" (32/8 heads, D 128, page size
 4) in bf16, NHD and HND pages of sizes 1..32, head ratios 1/2/4/8, head_dim
 64/128, causal / none / custom masks, ragged K/V, mixed decode + prefill
-batches, every split mode, and the append-prefill and ragged-mask workloads
-at full size (sampled rows against the oracle).
+batches, every split mode, and the append-prefill, mixed-step and ragged-mask
+workloads at full size (against the oracle on the first and last token of
+every query tile of every work item of the real plan).
 """
 import numpy as np
 import pytest

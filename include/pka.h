@@ -124,7 +124,8 @@ typedef struct pka_params {
    * g qo heads of a row packed into its 128-row tile ("Deep Dive -
    * FlashInfer": decode through the tensor-core tile for grouped heads);
    * 0: they go to the decode kernel (warp-level MMAs, faster for decode on
-   * GB300).  bf16 K/V, no graph mode. */
+   * GB300).  Over e4m3 pools such rows read the bf16 scratch like the other
+   * tensor-core rows (and count against graph_max_kv_tokens in graph mode). */
   int32_t decode_on_tensor_cores;
   int32_t reserved[1];         /* must be zero                                  */
 } pka_params;

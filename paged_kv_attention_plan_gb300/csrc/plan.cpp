@@ -123,8 +123,6 @@ pka_status check_supported(const pka_params* p) {
   if (g != 1 && g != 2 && g != 4 && g != 8) return PKA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128) return PKA_ERR_UNSUPPORTED;
   if (p->graph_max_batch > 0 && p->split_mode == PKA_SPLIT_FIXED) return PKA_ERR_UNSUPPORTED;
-  if (p->decode_on_tensor_cores && (p->graph_max_batch > 0 || p->kv_dtype != PKA_KV_BF16))
-    return PKA_ERR_UNSUPPORTED;
   return PKA_OK;
 }
 
@@ -229,8 +227,9 @@ pka_status derive(const pka_params* p, int32_t batch, const int32_t* qo, const i
 pka_status check_kv_dtype(const pka_params* p, const Batch& b) {
   if (p->kv_dtype != PKA_KV_FP8_E4M3 || !graph_mode(p) || p->graph_max_kv_tokens > 0)
     return PKA_OK;
+  const int32_t tc_rows = p->decode_on_tensor_cores ? 1 : 2;  // rows the tensor-core kernel takes
   for (int32_t q : b.qo_len)
-    if (q >= 2) {
+    if (q >= tc_rows) {
       pka::set_last_error("graph mode over e4m3 pools with qo_len >= 2 rows needs graph_max_kv_tokens");
       return PKA_ERR_UNSUPPORTED;
     }

@@ -68,3 +68,16 @@ def test_tc_batch_decode_full_size():
     o, lse, info = run_gpu(b, ("auto", 1), **TC)
     assert info.num_decode_items == 0
     assert_parity(o, lse, *run_oracle(b))
+
+
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+def test_tc_decode_e4m3(layout):
+    """Decode rows on the tensor-core kernel over e4m3 pools: every request's
+    keys are decoded to the bf16 scratch, which the tile reads as ragged K/V."""
+    qo = np.array([1, 1, 37, 1, 1], np.int32)
+    kv = np.array([300, 1, 60, 2000, 17], np.int32)
+    b = W.make_paged_batch(41, qo, kv, page_size=16, layout=layout, hq=32, hk=8, d=128,
+                           kv_dtype="e4m3", k_scale=0.5, v_scale=1.5)
+    o, lse, info = run_gpu(b, **TC)
+    assert info.num_decode_items == 0 and info.kv_scratch_rows == int(kv.sum())
+    assert_parity(o, lse, *run_oracle(b))

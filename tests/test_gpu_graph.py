@@ -65,8 +65,10 @@ PAGED_SPECS = [
 ]
 
 
-@pytest.mark.parametrize("layout,page_size", [("HND", 16), ("NHD", 1)])
-def test_graph_mode_capture_serves_new_plans(layout, page_size):
+@pytest.mark.parametrize("layout,page_size,tc", [("HND", 16, False), ("NHD", 1, False),
+                                                ("HND", 16, True)])
+def test_graph_mode_capture_serves_new_plans(layout, page_size, tc):
+    """tc: decode rows on the tensor-core kernel too (one launch for every row)."""
     hq, hk, d = 32, 8, 128
     max_batch, max_rows = 8, 640
     pool_pages = (20000 + page_size - 1) // page_size + 8 * 2
@@ -83,7 +85,8 @@ def test_graph_mode_capture_serves_new_plans(layout, page_size):
     attn = pka.BatchAttention()
     stream = torch.cuda.Stream()
     kw = dict(num_qo_heads=hq, num_kv_heads=hk, head_dim=d, page_size=page_size, layout=layout,
-              graph_max_batch=max_batch, graph_max_qo_rows=max_rows, stream=stream)
+              graph_max_batch=max_batch, graph_max_qo_rows=max_rows, decode_on_tensor_cores=tc,
+              stream=stream)
 
     def load(b):
         q_buf[:b.nnz_q].copy_(bf16(b.q))

@@ -468,7 +468,8 @@ def test_decode_rows_on_tensor_cores_plan(cfg):
     """With decode_on_tensor_cores, rows with qo_len == 1 become tensor-core
     items (one query token, the g heads of each kv head packed into the tile)
     whose key ranges tile [0, kv_len) per (request, kv head); the decode list
-    is empty.  Graph mode and e4m3 K/V refuse the option."""
+    is empty.  Graph mode keeps one layout with the option; over e4m3 pools the
+    rows read the bf16 scratch (in graph mode within graph_max_kv_tokens)."""
     b = CONFIGS[cfg]()
     hq, hk = b.num_qo_heads, b.num_kv_heads
     params = pka.make_params(hq, hk, b.head_dim, b.page_size, b.layout, b.mask_mode,
@@ -492,11 +493,23 @@ def test_decode_rows_on_tensor_cores_plan(cfg):
             assert _ranges_tile([(i["t0"], i["t1"]) for i in its], int(b.kv_lens[r]))
     g = pka.make_params(hq, hk, b.head_dim, b.page_size, b.layout, b.mask_mode,
                         decode_on_tensor_cores=True, graph_max_batch=len(b.kv_lens),
-                        graph_max_qo_rows=int(b.nnz_q))
-    assert pka.pka_validate(g, b.qo_indptr, b.kv_indptr, b.last_page_len) == UNSUPPORTED
+                        graph_max_qo_rows=int(b.nnz_q), num_sms=152)
+    assert pka.pka_validate(g, b.qo_indptr, b.kv_indptr, b.last_page_len) == OK
+    h = pka.pka_plan_create()
+    assert pka.pka_plan(h, g, qo, b.kv_indptr, b.last_page_len, None, buf, check=False) == OK
+    assert pka.pka_plan_get_info(h).num_decode_items == 0
+    # e4m3: every row (decode rows too) reads the bf16 scratch of its request
     f = pka.make_params(hq, hk, b.head_dim, b.page_size, b.layout, b.mask_mode,
-                        decode_on_tensor_cores=True, kv_dtype="e4m3")
-    assert pka.pka_validate(f, b.qo_indptr, b.kv_indptr, b.last_page_len) == UNSUPPORTED
+                        decode_on_tensor_cores=True, kv_dtype="e4m3", num_sms=152)
+    assert pka.pka_plan(h, f, qo, b.kv_indptr, b.last_page_len, None, buf, check=False) == OK
+    assert pka.pka_plan_get_info(h).kv_scratch_rows == int(np.sum(b.kv_lens))
+    fg = pka.make_params(hq, hk, b.head_dim, b.page_size, b.layout, b.mask_mode,
+                         decode_on_tensor_cores=True, kv_dtype="e4m3",
+                         graph_max_batch=len(b.kv_lens), graph_max_qo_rows=int(b.nnz_q))
+    assert pka.pka_validate(fg, b.qo_indptr, b.kv_indptr, b.last_page_len) == UNSUPPORTED
+    fg.graph_max_kv_tokens = int(np.sum(b.kv_lens))
+    assert pka.pka_plan(h, fg, qo, b.kv_indptr, b.last_page_len, None, buf, check=False) == OK
+    pka.pka_plan_destroy(h)
 
 
 @pytest.mark.parametrize("qo,kv,last", [([0], [0], []), ([0, 0, 0], [0, 2, 3], [3, 1])])
